@@ -1,0 +1,199 @@
+"""ctypes binding of libspark_attn.so (include/spark_attn.h).
+
+Argument marshalling only: every step of the attention core runs in the CUDA
+library.  PyTorch supplies device memory and the current stream.  There is no
+fallback: if the library is missing, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+HEAD_DIM = 256
+
+SPARK_OK = 0
+SPARK_ERR_NULL = 1
+SPARK_ERR_SHAPE = 2
+SPARK_ERR_UNSUPPORTED = 3
+SPARK_ERR_ALIGN = 4
+SPARK_ERR_CAPACITY = 5
+SPARK_ERR_WORKSPACE = 6
+SPARK_ERR_CUDA = 7
+SPARK_ERR_DEVICE = 8
+
+SPARK_LAYER_FULL = 0
+SPARK_LAYER_SLIDING = 1
+SPARK_GATE_SIGMOID = 0
+
+SPARK_DEVERR_POSITION = 0x1
+SPARK_DEVERR_TIMEOUT = 0x2
+
+
+class spark_layer_desc(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("window", ctypes.c_int32),
+                ("rope_theta", ctypes.c_double), ("rot_dim", ctypes.c_int32),
+                ("gate_mode", ctypes.c_int32)]
+
+
+def _load() -> ctypes.CDLL:
+    path = _build.LIB_PATH
+    if not os.path.exists(path):
+        raise ImportError(
+            f"the CUDA library {path} is not built; run "
+            "`python -c 'import __graft_entry__ as g; g.build()'` first")
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    i32, i64, sz = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    D = ctypes.POINTER(spark_layer_desc)
+    lib.spark_attn_prefill_workspace_size.argtypes = [i32, i32, i32, i32, D]
+    lib.spark_attn_prefill_workspace_size.restype = sz
+    lib.spark_attn_prefill.argtypes = [P, P, P, D, i32, i32, i32, i32, P, P, sz, P]
+    lib.spark_attn_prefill.restype = i32
+    lib.spark_attn_decode_workspace_size.argtypes = [i32, i32, i32, i64, D]
+    lib.spark_attn_decode_workspace_size.restype = sz
+    lib.spark_attn_decode.argtypes = [P, P, P, P, P, i64, D, i32, i32, i32, P, P, sz, P]
+    lib.spark_attn_decode.restype = i32
+    lib.spark_attn_read_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), i32, P]
+    lib.spark_attn_read_status.restype = i32
+    lib.spark_status_str.argtypes = [i32]
+    lib.spark_status_str.restype = ctypes.c_char_p
+    lib.spark_attn_version.argtypes = []
+    lib.spark_attn_version.restype = ctypes.c_char_p
+    return lib
+
+
+lib = _load()
+
+
+class SparkError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({spark_status_str(status)})")
+
+
+def spark_status_str(status: int) -> str:
+    return lib.spark_status_str(status).decode()
+
+
+def spark_attn_version() -> str:
+    return lib.spark_attn_version().decode()
+
+
+def layer_desc(kind: int, window: int, rope_theta: float, rot_dim: int,
+               gate_mode: int = SPARK_GATE_SIGMOID) -> spark_layer_desc:
+    return spark_layer_desc(kind, window, float(rope_theta), rot_dim, gate_mode)
+
+
+def as_desc(layer) -> spark_layer_desc:
+    """Accepts a spark_layer_desc or any object with kind/window/theta/rot_dim."""
+    if isinstance(layer, spark_layer_desc):
+        return layer
+    return layer_desc(layer.kind, layer.window, layer.theta, layer.rot_dim,
+                      getattr(layer, "gate_mode", SPARK_GATE_SIGMOID))
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t: torch.Tensor, dtype, name: str):
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA {dtype} tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def spark_attn_prefill_workspace_size(B: int, T: int, H: int, Hkv: int, layer) -> int:
+    d = as_desc(layer)
+    return lib.spark_attn_prefill_workspace_size(B, T, H, Hkv, ctypes.byref(d))
+
+
+def spark_attn_decode_workspace_size(B: int, H: int, Hkv: int, cap: int, layer) -> int:
+    d = as_desc(layer)
+    return lib.spark_attn_decode_workspace_size(B, H, Hkv, cap, ctypes.byref(d))
+
+
+def new_workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A zeroed workspace (the status word must start at 0)."""
+    return torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def spark_attn_prefill(qkv: torch.Tensor, gate: torch.Tensor, pos: torch.Tensor, layer,
+                       out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                       stream=None) -> torch.Tensor:
+    """Prefill: qkv bf16 [B,T,(H+2Hkv)*256], gate fp32 [B,T,H], pos int32 [B,T]
+    -> out bf16 [B,T,H*256]."""
+    _need(qkv, torch.bfloat16, "qkv")
+    _need(gate, torch.float32, "gate")
+    _need(pos, torch.int32, "pos")
+    B, T, W = qkv.shape
+    H = gate.shape[-1]
+    Hkv = (W // HEAD_DIM - H) // 2
+    if gate.shape != (B, T, H) or pos.shape != (B, T) or (H + 2 * Hkv) * HEAD_DIM != W:
+        raise ValueError("inconsistent prefill shapes")
+    d = as_desc(layer)
+    if out is None:
+        out = torch.empty((B, T, H * HEAD_DIM), dtype=torch.bfloat16, device=qkv.device)
+    _need(out, torch.bfloat16, "out")
+    need = lib.spark_attn_prefill_workspace_size(B, T, H, Hkv, ctypes.byref(d))
+    if workspace is None:
+        workspace = new_workspace(need, qkv.device)
+    st = lib.spark_attn_prefill(_ptr(qkv), _ptr(gate), _ptr(pos), ctypes.byref(d), B, T, H,
+                                Hkv, _ptr(out), _ptr(workspace), workspace.numel(),
+                                _stream(stream))
+    if st != SPARK_OK:
+        raise SparkError(st, "spark_attn_prefill")
+    return out
+
+
+def spark_attn_decode(qkv: torch.Tensor, gate: torch.Tensor, pos: torch.Tensor,
+                      k_cache: torch.Tensor, v_cache: torch.Tensor, layer,
+                      out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                      stream=None) -> torch.Tensor:
+    """One decode step: qkv bf16 [B,(H+2Hkv)*256], gate fp32 [B,H], pos int32 [B],
+    caches bf16 [B,Hkv,cap,256] (updated in place) -> out bf16 [B,H*256]."""
+    _need(qkv, torch.bfloat16, "qkv")
+    _need(gate, torch.float32, "gate")
+    _need(pos, torch.int32, "pos")
+    _need(k_cache, torch.bfloat16, "k_cache")
+    _need(v_cache, torch.bfloat16, "v_cache")
+    B, W = qkv.shape
+    H = gate.shape[-1]
+    Hkv = (W // HEAD_DIM - H) // 2
+    if (gate.shape != (B, H) or pos.shape != (B,) or k_cache.shape != v_cache.shape
+            or k_cache.shape[:2] != (B, Hkv) or k_cache.shape[3] != HEAD_DIM):
+        raise ValueError("inconsistent decode shapes")
+    cap = k_cache.shape[2]
+    d = as_desc(layer)
+    if out is None:
+        out = torch.empty((B, H * HEAD_DIM), dtype=torch.bfloat16, device=qkv.device)
+    _need(out, torch.bfloat16, "out")
+    need = lib.spark_attn_decode_workspace_size(B, H, Hkv, cap, ctypes.byref(d))
+    if workspace is None:
+        workspace = new_workspace(need, qkv.device)
+    st = lib.spark_attn_decode(_ptr(qkv), _ptr(gate), _ptr(pos), _ptr(k_cache), _ptr(v_cache),
+                               cap, ctypes.byref(d), B, H, Hkv, _ptr(out), _ptr(workspace),
+                               workspace.numel(), _stream(stream))
+    if st != SPARK_OK:
+        raise SparkError(st, "spark_attn_decode")
+    return out
+
+
+def spark_attn_read_status(workspace: torch.Tensor, clear: bool = False, stream=None) -> int:
+    """The sticky device status word of a workspace (synchronizes)."""
+    v = ctypes.c_uint32(0)
+    st = lib.spark_attn_read_status(_ptr(workspace), ctypes.byref(v), int(clear),
+                                    _stream(stream))
+    if st != SPARK_OK:
+        raise SparkError(st, "spark_attn_read_status")
+    return v.value

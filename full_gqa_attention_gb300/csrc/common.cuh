@@ -1,0 +1,97 @@
+// common.cuh -- constants, launch parameters and the RoPE angle helper shared
+// by the kernels of the attention core.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace spark {
+
+constexpr int kHeadDim = 256;
+constexpr int kMaxRopePairs = kHeadDim / 2;
+constexpr int kLayerFull = 0;
+constexpr int kLayerSliding = 1;
+
+// log2(e) / sqrt(256): scores are kept in base-2 units, s * kScaleLog2.
+constexpr float kScaleLog2 = 1.4426950408889634f / 16.0f;
+
+// Bytes reserved at the start of every workspace for the status word.
+constexpr size_t kWorkspaceHeader = 256;
+
+// RoPE frequencies of one layer type, in turns per position:
+// u_k = theta^(-2k/r) / (2 pi), stored as an unevaluated fp32 sum hi + lo
+// (computed on the host in fp64).
+struct RopeTable {
+    float2 u[kMaxRopePairs];
+    int rot_dim;
+};
+
+// cos and sin of the RoPE angle of one pair at an integer position.
+//
+// The angle pos * inv_freq reaches 1e6 rad at the 1M-token positions of the
+// full layers, where a plain fp32 product is off by up to ~0.03 rad.  Instead
+// the angle is taken in turns and reduced exactly: with fp = pos (exact below
+// 2^24) and u = u_hi + u_lo,
+//   p = fl(fp * u_hi),  e = fp * u_hi - p  (exact, by fma),
+//   p - rint(p)         (exact: p and its nearest integer share the exponent),
+//   t = (p - rint(p)) + (fp * u_lo + e)   in [-1/2, 1/2] up to rounding,
+// so only the last two roundings (~2^-25 turns, ~2e-7 rad) remain before
+// sincospif.  Explicit _rn intrinsics keep the compiler from fusing the
+// products into neighbouring adds, which would count e twice.
+__device__ __forceinline__ void rope_cos_sin(int pos, float2 u, float &c, float &s) {
+    const float fp = static_cast<float>(pos);
+    const float p = __fmul_rn(fp, u.x);
+    const float e = __fmaf_rn(fp, u.x, -p);
+    const float f = __fsub_rn(p, rintf(p));
+    const float t = __fadd_rn(f, __fmaf_rn(fp, u.y, e));
+    sincospif(__fmul_rn(2.0f, t), &s, &c);
+}
+
+// Rotates one (x1, x2) pair: y1 = x1 c - x2 s, y2 = x2 c + x1 s.
+__device__ __forceinline__ void rope_rotate(float x1, float x2, float c, float s, float &y1,
+                                            float &y2) {
+    y1 = __fsub_rn(__fmul_rn(x1, c), __fmul_rn(x2, s));
+    y2 = __fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, s));
+}
+
+__device__ __forceinline__ float sigmoid_f32(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+// ---------------------------------------------------------------- decode
+
+struct DecodeParams {
+    const __nv_bfloat16 *qkv;  // [B, (H+2Hkv)*256]
+    const float *gate;         // [B, H]
+    const int32_t *pos;        // [B]
+    __nv_bfloat16 *k_cache;    // [B, Hkv, cap, 256]
+    __nv_bfloat16 *v_cache;    // [B, Hkv, cap, 256]
+    __nv_bfloat16 *out;        // [B, H*256]
+    float *part_ml;            // [B, H, nsplit, 2]: running max (base-2 units), sum
+    float *part_o;             // [B, H, nsplit, 256]: unnormalised output
+    unsigned *status;          // device status word
+    long long cap;             // cache slots per (b, kv head)
+    int B, H, Hkv, G;
+    int kind, window;
+    int nsplit;                // splits per (b, kv head)
+    int chunk;                 // scanned slots per split (multiple of 64)
+    RopeTable rope;
+};
+
+// ---------------------------------------------------------------- prefill
+
+struct PrefillParams {
+    const __nv_bfloat16 *qkv;  // [B, T, (H+2Hkv)*256]
+    const float *gate;         // [B, T, H]
+    const int32_t *pos;        // [B, T]
+    __nv_bfloat16 *krot;       // [B, Hkv, T, rot_w]: rotated leading dims of K
+    unsigned *status;
+    int B, T, H, Hkv, G;
+    int kind, window;
+    int rot_w;                 // rot_dim rounded up to 64: leading K dims read from krot
+    int n_qtiles;              // query tiles per (b, kv head)
+    RopeTable rope;
+};
+
+}  // namespace spark

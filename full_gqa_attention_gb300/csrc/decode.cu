@@ -1,0 +1,435 @@
+// decode.cu -- one decode step of the gated GQA attention core.
+//
+// Spark-X2.5 architecture (4B / 1.7B), §3 Eq. 1 (softmax(QK^T/16) V times the
+// per-head sigmoid gate) and §4 (layered RoPE); the cache behaviour is the one
+// the Spark-X2.5-4B hybrid-attention explainer (lshu.cn) describes: full
+// layers keep every token, sliding layers only the latest `window`.
+//
+// Two kernels on one stream:
+//   decode_split_kernel  grid (nsplit, Hkv, B).  Each CTA streams a chunk of
+//       cache slots of one (sequence, KV head) through a TMA ring in shared
+//       memory and keeps an online softmax for the G query heads of the group
+//       (scores and P*V on the tensor cores, keys in the M dimension).  It
+//       writes one partial state (running max, sum, unnormalised output) per
+//       head.
+//   decode_merge_kernel  grid (Hkv, B).  Rotates q and the new key, scores the
+//       new token, merges it with the partial states (log-sum-exp rescale),
+//       applies the gate, and stores the new key/value at slot(pos).
+// The new token is not read from the cache by the split kernel, so the cache
+// write can come last without a race: on a full layer slot(pos) lies past
+// every cached token, and on a ring it holds token pos - cap, which is out of
+// the window (cap >= window).
+#include "common.cuh"
+
+namespace spark {
+
+constexpr int kDecTile = 64;                              // cache slots per stage
+constexpr int kDecStages = 3;
+constexpr int kDecWarps = 4;                              // consumers, 16 slots each
+constexpr int kDecThreads = (kDecWarps + 1) * 32;         // + one producer warp
+constexpr int kDecTileBytes = kDecTile * kHeadDim * 2;    // 32 KB (K or V)
+constexpr int kDecStageBytes = 2 * kDecTileBytes;         // K + V
+constexpr int kDecQBytes = 8 * kHeadDim * 2;              // 8 (padded) query heads
+constexpr int kDecSmemBytes = 1024 + kDecStages * kDecStageBytes + kDecQBytes +
+                              2 * kDecStages * 8;
+
+// Slot s (s < min(pos, cap)) of a ring of `cap` slots holds the latest token
+// j < pos with j = s (mod cap).  It is visible from the new token at `pos`
+// iff pos - j < window.
+__device__ __forceinline__ bool ring_slot_visible(long long s, long long pos, long long cap,
+                                                  int window) {
+    const long long j = s + cap * ((pos - 1 - s) / cap);
+    return pos - j < (long long)window;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__global__ void __launch_bounds__(kDecThreads, 1)
+    decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v,
+                        const __grid_constant__ DecodeParams P) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *stages = smem;
+    __nv_bfloat16 *qs = reinterpret_cast<__nv_bfloat16 *>(smem + kDecStages * kDecStageBytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kDecStages * kDecStageBytes + kDecQBytes);
+    uint64_t *empty = full + kDecStages;
+    __shared__ int abort_flag;
+    __shared__ float red_m[kDecWarps][8];
+    __shared__ float red_l[kDecWarps][8];
+
+    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    const long long p = P.pos[b];
+    if (p < 0 || (P.kind == kLayerFull && p >= P.cap)) {
+        if (split == 0 && g == 0 && tid == 0) atomicOr(P.status, kErrPosition);
+        return;
+    }
+    // Scanned slots: full layer -> tokens [0, pos); ring -> slots [0, min(pos, cap)).
+    const long long n_scan = (P.kind == kLayerFull) ? p : (p < P.cap ? p : P.cap);
+    const long long c_lo = static_cast<long long>(split) * P.chunk;
+    const long long c_hi = (c_lo + P.chunk < n_scan) ? c_lo + P.chunk : n_scan;
+    if (c_lo >= c_hi) return;  // empty split: the merge does not read it
+    const int ntiles = static_cast<int>((c_hi - c_lo + kDecTile - 1) / kDecTile);
+
+    if (tid == 0) {
+        for (int s = 0; s < kDecStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kDecWarps);
+        }
+        fence_mbar_init();
+        abort_flag = 0;
+    }
+    if (warp == kDecWarps && lane == 0) {
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+    }
+
+    // The group's G query heads, rotated and rounded to bf16 (heads G..7 zero).
+    const size_t width = static_cast<size_t>(P.H + 2 * P.Hkv) * kHeadDim;
+    for (int i = tid; i < 8 * (kHeadDim / 8); i += kDecThreads) {
+        const int hh = i / (kHeadDim / 8), v = i % (kHeadDim / 8);
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (hh < P.G)
+            val = *reinterpret_cast<const uint4 *>(
+                P.qkv + b * width + static_cast<size_t>(g * P.G + hh) * kHeadDim + v * 8);
+        *reinterpret_cast<uint4 *>(qs + hh * kHeadDim + v * 8) = val;
+    }
+    __syncthreads();
+    const int half = P.rope.rot_dim / 2;
+    for (int k = tid; k < half; k += kDecThreads) {
+        float c, s;
+        rope_cos_sin(static_cast<int>(p), P.rope.u[k], c, s);
+        for (int hh = 0; hh < P.G; ++hh) {
+            const float x1 = __bfloat162float(qs[hh * kHeadDim + k]);
+            const float x2 = __bfloat162float(qs[hh * kHeadDim + k + half]);
+            float y1, y2;
+            rope_rotate(x1, x2, c, s, y1, y2);
+            qs[hh * kHeadDim + k] = __float2bfloat16_rn(y1);
+            qs[hh * kHeadDim + k + half] = __float2bfloat16_rn(y2);
+        }
+    }
+    __syncthreads();
+
+    if (warp == kDecWarps) {
+        // ------------------------------------------------------ TMA producer
+        int issued = 0;
+        if (lane == 0) {
+            for (int t = 0; t < ntiles; ++t) {
+                const int s = t % kDecStages;
+                if (t >= kDecStages &&
+                    !mbar_wait(&empty[s], ((t / kDecStages) - 1) & 1, &abort_flag, P.status))
+                    break;
+                mbar_arrive_expect_tx(&full[s], kDecStageBytes);
+                const int key0 = static_cast<int>(c_lo + static_cast<long long>(t) * kDecTile);
+                uint8_t *kt = stages + s * kDecStageBytes;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    tma_load_4d(kt + c * (kDecTileBytes / 4), &tm_k, &full[s], c * 64, key0, g, b);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    tma_load_4d(kt + kDecTileBytes + c * (kDecTileBytes / 4), &tm_v, &full[s],
+                                c * 64, key0, g, b);
+                ++issued;
+            }
+        }
+        __syncwarp();
+        __syncthreads();
+        // Copies still in flight after an abort must land before the CTA
+        // releases its shared memory.
+        if (lane == 0 && abort_flag) {
+            const int first = issued > kDecStages ? issued - kDecStages : 0;
+            for (int t = first; t < issued; ++t)
+                mbar_wait_plain(&full[t % kDecStages], (t / kDecStages) & 1);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    // Q^T as the B operand of S^T = K Q^T: one (b0, b1) pair per 16 dims.
+    uint32_t qf[16][2];
+    {
+        const uint32_t qbase = smem_u32(qs);
+#pragma unroll
+        for (int ks = 0; ks < 16; ks += 2) {
+            const uint32_t addr = qbase + (lane & 7) * (kHeadDim * 2) +
+                                  (ks * 16 + (lane >> 3) * 8) * 2;
+            ldmatrix_x4(addr, qf[ks][0], qf[ks][1], qf[ks + 1][0], qf[ks + 1][1]);
+        }
+    }
+
+    float o[16][4];
+#pragma unroll
+    for (int db = 0; db < 16; ++db) o[db][0] = o[db][1] = o[db][2] = o[db][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    const int arow = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;  // K rows (ldmatrix)
+    const int vrow = warp * 16 + (lane & 7) + (lane >> 4) * 8;        // V rows (ldmatrix.trans)
+
+    for (int t = 0; t < ntiles; ++t) {
+        const int s = t % kDecStages;
+        if (!mbar_wait(&full[s], (t / kDecStages) & 1, &abort_flag, P.status)) break;
+        const uint32_t kt = smem_u32(stages + s * kDecStageBytes);
+        const uint32_t vt = kt + kDecTileBytes;
+
+        // S^T (16 slots x 8 heads) = K (16 x 256) Q^T (256 x 8)
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 16; ++ks) {
+            const int gran = ((ks * 16) & 63) / 8 + (lane >> 4);
+            const uint32_t addr = kt + (ks >> 2) * (kDecTileBytes / 4) + arow * 128 +
+                                  ((gran ^ (arow & 7)) << 4);
+            uint32_t a0, a1, a2, a3;
+            ldmatrix_x4(addr, a0, a1, a2, a3);
+            mma_bf16_16816(sc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+        }
+
+        // this thread's two slots (rows lane/4 and lane/4 + 8) and two heads
+        const long long sa = c_lo + static_cast<long long>(t) * kDecTile + warp * 16 + (lane >> 2);
+        const long long sb = sa + 8;
+        bool va = sa < c_hi, vb = sb < c_hi;
+        if (P.kind == kLayerSliding) {
+            va = va && ring_slot_visible(sa, p, P.cap, P.window);
+            vb = vb && ring_slot_visible(sb, p, P.cap, P.window);
+        }
+        const float x0 = va ? sc[0] * kScaleLog2 : -INFINITY;
+        const float x1 = va ? sc[1] * kScaleLog2 : -INFINITY;
+        const float x2 = vb ? sc[2] * kScaleLog2 : -INFINITY;
+        const float x3 = vb ? sc[3] * kScaleLog2 : -INFINITY;
+        float t0 = fmaxf(x0, x2), t1 = fmaxf(x1, x3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, off));
+            t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, off));
+        }
+        const float n0 = fmaxf(m0, t0), n1 = fmaxf(m1, t1);
+        const float r0 = (n0 == -INFINITY) ? 1.f : fast_exp2(m0 - n0);
+        const float r1 = (n1 == -INFINITY) ? 1.f : fast_exp2(m1 - n1);
+        const float z0 = (n0 == -INFINITY) ? 0.f : n0;
+        const float z1 = (n1 == -INFINITY) ? 0.f : n1;
+        const float p0 = fast_exp2(x0 - z0), p1 = fast_exp2(x1 - z1);
+        const float p2 = fast_exp2(x2 - z0), p3 = fast_exp2(x3 - z1);
+        l0 = l0 * r0 + p0 + p2;
+        l1 = l1 * r1 + p1 + p3;
+        m0 = n0;
+        m1 = n1;
+#pragma unroll
+        for (int db = 0; db < 16; ++db) {
+            o[db][0] *= r0;
+            o[db][1] *= r1;
+            o[db][2] *= r0;
+            o[db][3] *= r1;
+        }
+        // P^T as the B operand of O^T += V^T P^T (transpose of the score fragment)
+        const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
+        const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
+#pragma unroll
+        for (int db = 0; db < 16; ++db) {
+            const int gran = ((db * 16) & 63) / 8 + ((lane >> 3) & 1);
+            const uint32_t addr = vt + (db >> 2) * (kDecTileBytes / 4) + vrow * 128 +
+                                  ((gran ^ (vrow & 7)) << 4);
+            uint32_t a0, a1, a2, a3;
+            ldmatrix_x4_trans(addr, a0, a1, a2, a3);
+            mma_bf16_16816(o[db], a0, a1, a2, a3, pb0, pb1);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+
+    // row sums over the 8 lanes that share this thread's heads
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    const int h0 = 2 * (lane & 3), h1 = h0 + 1;
+    if (lane < 4) {
+        red_m[warp][h0] = m0;
+        red_m[warp][h1] = m1;
+        red_l[warp][h0] = l0;
+        red_l[warp][h1] = l1;
+    }
+    named_bar_sync(1, kDecWarps * 32);
+    // abort_flag is stable here: it is only raised inside a wait, and every
+    // wait of the producer and the consumers has returned.
+    if (!abort_flag) {
+        float M0 = red_m[0][h0], M1 = red_m[0][h1];
+#pragma unroll
+        for (int w = 1; w < kDecWarps; ++w) {
+            M0 = fmaxf(M0, red_m[w][h0]);
+            M1 = fmaxf(M1, red_m[w][h1]);
+        }
+        const float s0 = (M0 == -INFINITY) ? 0.f : fast_exp2(m0 - M0);
+        const float s1 = (M1 == -INFINITY) ? 0.f : fast_exp2(m1 - M1);
+        // every stage has been consumed: the ring is free for the reduction
+        float *red_o = reinterpret_cast<float *>(stages);
+#pragma unroll
+        for (int db = 0; db < 16; ++db) {
+            const int d = db * 16 + (lane >> 2);
+            red_o[(warp * 8 + h0) * kHeadDim + d] = o[db][0] * s0;
+            red_o[(warp * 8 + h1) * kHeadDim + d] = o[db][1] * s1;
+            red_o[(warp * 8 + h0) * kHeadDim + d + 8] = o[db][2] * s0;
+            red_o[(warp * 8 + h1) * kHeadDim + d + 8] = o[db][3] * s1;
+        }
+        named_bar_sync(1, kDecWarps * 32);
+        const size_t part0 = (static_cast<size_t>(b) * P.H + static_cast<size_t>(g) * P.G) * P.nsplit;
+        for (int i = tid; i < P.G * kHeadDim; i += kDecWarps * 32) {
+            const int hh = i / kHeadDim, d = i % kHeadDim;
+            float acc = 0.f;
+#pragma unroll
+            for (int w = 0; w < kDecWarps; ++w) acc += red_o[(w * 8 + hh) * kHeadDim + d];
+            P.part_o[(part0 + static_cast<size_t>(hh) * P.nsplit + split) * kHeadDim + d] = acc;
+        }
+        if (tid < P.G) {
+            const int hh = tid;
+            float M = red_m[0][hh];
+            for (int w = 1; w < kDecWarps; ++w) M = fmaxf(M, red_m[w][hh]);
+            float L = 0.f;
+            if (M != -INFINITY)
+                for (int w = 0; w < kDecWarps; ++w) L += red_l[w][hh] * fast_exp2(red_m[w][hh] - M);
+            float2 ml = make_float2(M, L);
+            *reinterpret_cast<float2 *>(P.part_ml + 2 * (part0 + static_cast<size_t>(hh) * P.nsplit +
+                                                         split)) = ml;
+        }
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant__ DecodeParams P) {
+    const int g = blockIdx.x, b = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp >= P.G) return;
+    const int h = g * P.G + warp;
+    const long long p = P.pos[b];
+    if (p < 0 || (P.kind == kLayerFull && p >= P.cap)) {
+        if (g == 0 && threadIdx.x == 0) atomicOr(P.status, kErrPosition);
+        return;
+    }
+    const size_t width = static_cast<size_t>(P.H + 2 * P.Hkv) * kHeadDim;
+    const __nv_bfloat16 *row = P.qkv + b * width;
+    const uint4 qv = *reinterpret_cast<const uint4 *>(row + static_cast<size_t>(h) * kHeadDim + lane * 8);
+    const uint4 kv = *reinterpret_cast<const uint4 *>(row + static_cast<size_t>(P.H + g) * kHeadDim + lane * 8);
+    const uint4 vv = *reinterpret_cast<const uint4 *>(row + static_cast<size_t>(P.H + P.Hkv + g) * kHeadDim + lane * 8);
+    const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+    const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
+    const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
+    float q[8], k[8], v[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        q[2 * i] = bf16_lo(qw[i]);
+        q[2 * i + 1] = bf16_hi(qw[i]);
+        k[2 * i] = bf16_lo(kw[i]);
+        k[2 * i + 1] = bf16_hi(kw[i]);
+        v[2 * i] = bf16_lo(vw[i]);
+        v[2 * i + 1] = bf16_hi(vw[i]);
+    }
+
+    // RoPE of this lane's 8 dims d0..d0+7; the partner dims d -/+ r/2 live in
+    // the lane r/16 away (r/2 is a multiple of 8).
+    const int r = P.rope.rot_dim, half = r / 2, d0 = lane * 8;
+    if (r > 0) {
+        const int partner = (d0 >= r) ? lane : (d0 < half ? lane + half / 8 : lane - half / 8);
+        float qp[8], kp[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            qp[i] = __shfl_sync(0xffffffffu, q[i], partner);
+            kp[i] = __shfl_sync(0xffffffffu, k[i], partner);
+        }
+        if (d0 < r) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int kk = (d0 < half) ? d0 + i : d0 + i - half;
+                float c, s;
+                rope_cos_sin(static_cast<int>(p), P.rope.u[kk], c, s);
+                float y1, y2;
+                if (d0 < half) {
+                    rope_rotate(q[i], qp[i], c, s, y1, y2);
+                    q[i] = y1;
+                    rope_rotate(k[i], kp[i], c, s, y1, y2);
+                    k[i] = y1;
+                } else {
+                    rope_rotate(qp[i], q[i], c, s, y1, y2);
+                    q[i] = y2;
+                    rope_rotate(kp[i], k[i], c, s, y1, y2);
+                    k[i] = y2;
+                }
+            }
+        }
+    }
+    uint32_t kb[4];
+    float dot = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        kb[i] = pack_bf16x2(k[2 * i], k[2 * i + 1]);
+        const uint32_t qb = pack_bf16x2(q[2 * i], q[2 * i + 1]);
+        dot = fmaf(bf16_lo(qb), bf16_lo(kb[i]), dot);
+        dot = fmaf(bf16_hi(qb), bf16_hi(kb[i]), dot);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+    const float x_new = dot * kScaleLog2;
+
+    // merge the new token with the partial states of the non-empty splits
+    const long long n_scan = (P.kind == kLayerFull) ? p : (p < P.cap ? p : P.cap);
+    const int nvalid = static_cast<int>((n_scan + P.chunk - 1) / P.chunk);
+    const size_t part0 = (static_cast<size_t>(b) * P.H + h) * P.nsplit;
+    float M = x_new;
+    for (int sp = 0; sp < nvalid; ++sp) M = fmaxf(M, P.part_ml[2 * (part0 + sp)]);
+    const float w_new = fast_exp2(x_new - M);
+    float L = w_new;
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = v[i] * w_new;
+    for (int sp = 0; sp < nvalid; ++sp) {
+        const float2 ml = *reinterpret_cast<const float2 *>(P.part_ml + 2 * (part0 + sp));
+        const float w = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
+        L += ml.y * w;
+        const float4 *po = reinterpret_cast<const float4 *>(P.part_o + (part0 + sp) * kHeadDim + d0);
+        const float4 a = po[0], c = po[1];
+        acc[0] += a.x * w;
+        acc[1] += a.y * w;
+        acc[2] += a.z * w;
+        acc[3] += a.w * w;
+        acc[4] += c.x * w;
+        acc[5] += c.y * w;
+        acc[6] += c.z * w;
+        acc[7] += c.w * w;
+    }
+    const float scale = sigmoid_f32(P.gate[static_cast<size_t>(b) * P.H + h]) / L;
+    uint4 ov;
+    ov.x = pack_bf16x2(acc[0] * scale, acc[1] * scale);
+    ov.y = pack_bf16x2(acc[2] * scale, acc[3] * scale);
+    ov.z = pack_bf16x2(acc[4] * scale, acc[5] * scale);
+    ov.w = pack_bf16x2(acc[6] * scale, acc[7] * scale);
+    *reinterpret_cast<uint4 *>(P.out + static_cast<size_t>(b) * P.H * kHeadDim +
+                               static_cast<size_t>(h) * kHeadDim + d0) = ov;
+
+    // write-then-attend: the new rotated key and its value go to slot(pos)
+    if (warp == 0) {
+        const long long slot = (P.kind == kLayerFull) ? p : p % P.cap;
+        const size_t off = ((static_cast<size_t>(b) * P.Hkv + g) * P.cap + slot) * kHeadDim + d0;
+        *reinterpret_cast<uint4 *>(P.k_cache + off) = make_uint4(kb[0], kb[1], kb[2], kb[3]);
+        *reinterpret_cast<uint4 *>(P.v_cache + off) = vv;
+    }
+}
+
+// ---------------------------------------------------------------- launchers
+
+cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeParams &P,
+                          cudaStream_t stream) {
+    cudaError_t err = cudaFuncSetAttribute(decode_split_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kDecSmemBytes);
+    if (err != cudaSuccess) return err;
+    dim3 grid(P.nsplit, P.Hkv, P.B);
+    decode_split_kernel<<<grid, kDecThreads, kDecSmemBytes, stream>>>(tm_k, tm_v, P);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    decode_merge_kernel<<<dim3(P.Hkv, P.B), 32 * P.G, 0, stream>>>(P);
+    return cudaGetLastError();
+}
+
+}  // namespace spark

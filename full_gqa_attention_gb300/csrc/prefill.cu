@@ -1,0 +1,492 @@
+// prefill.cu -- prefill of the gated GQA attention core on the 5th-generation
+// tensor cores (tcgen05, accumulators in TMEM, operands staged by TMA).
+//
+// Spark-X2.5 architecture (4B / 1.7B): §3 Eq. 1 (softmax(QK^T/16) V times the
+// per-head sigmoid gate), §4 layered RoPE, §2 causal / sliding-window masks.
+//
+// Two kernels on one stream:
+//   prefill_rope_k_kernel  writes the leading rot_w = roundup(rot_dim, 64)
+//       dims of every key, rotated, to a workspace [B][Hkv][T][rot_w].  The
+//       other key dims and all of V are read by TMA straight from qkv.
+//   prefill_attn_kernel    one CTA per (query tile, KV head, sequence).  A
+//       query tile is 128 rows = (128/G) tokens x the G query heads that share
+//       the KV head, so every K/V byte brought on chip serves all G heads.
+//       Warp roles:
+//         warp 0       TMA producer (Q tile once, then K and V through a ring
+//                      of 16 KB slots)
+//         warp 1       TMEM owner and MMA issuer (one thread)
+//         warps 4..7   softmax: thread i owns query row i (TMEM lane i)
+//       TMEM (512 columns): O [128 x 256 fp32] in columns 0..255, two score
+//       buffers S0/S1 [128 x 128 fp32] in 256..383 and 384..511.  The
+//       probabilities P (bf16) overwrite the first 64 columns of their score
+//       buffer and feed P*V as the TMEM A operand.  QK^T of tile j+1 runs on
+//       the tensor cores while the softmax of tile j runs on the CUDA cores.
+//       Q is rotated in shared memory by the softmax threads (each its own
+//       row) before the first product.  Key tiles wholly outside the causal
+//       band / window are never visited; boundary tiles are masked per element.
+//       Online softmax in base 2 with a lazy rescale: the reference maximum
+//       moves only when a row's maximum grows by more than 2^8.
+#include "common.cuh"
+
+namespace spark {
+
+// ---------------------------------------------------------------- K RoPE
+
+constexpr int kRopeThreads = 256;
+
+__global__ void __launch_bounds__(kRopeThreads) prefill_rope_k_kernel(
+    const __grid_constant__ PrefillParams P) {
+    const int r = P.rope.rot_dim, half = r / 2;
+    const int n_rot = half / 8;              // groups of 8 rotated pairs
+    const int n_copy = (P.rot_w - r) / 8;    // groups of 8 dims copied unrotated
+    const int items = n_rot + n_copy;
+    const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long row = idx / items;
+    const int it = static_cast<int>(idx % items);
+    if (row >= static_cast<long long>(P.B) * P.T) return;
+    const int b = static_cast<int>(row / P.T), t = static_cast<int>(row % P.T);
+    const size_t width = static_cast<size_t>(P.H + 2 * P.Hkv) * kHeadDim;
+    const __nv_bfloat16 *src = P.qkv + row * width + static_cast<size_t>(P.H) * kHeadDim;
+    __nv_bfloat16 *dst0 = P.krot + (static_cast<size_t>(b) * P.Hkv * P.T + t) * P.rot_w;
+    const size_t head_stride = static_cast<size_t>(P.T) * P.rot_w;
+    if (it < n_rot) {
+        const int k0 = it * 8;
+        const int p = P.pos[row];
+        float c[8], s[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rope_cos_sin(p, P.rope.u[k0 + i], c[i], s[i]);
+        for (int g = 0; g < P.Hkv; ++g) {
+            const uint4 a = *reinterpret_cast<const uint4 *>(src + g * kHeadDim + k0);
+            const uint4 bb = *reinterpret_cast<const uint4 *>(src + g * kHeadDim + k0 + half);
+            const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+            const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
+            uint32_t ya[4], yb[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float y1l, y2l, y1h, y2h;
+                rope_rotate(bf16_lo(aw[i]), bf16_lo(bw[i]), c[2 * i], s[2 * i], y1l, y2l);
+                rope_rotate(bf16_hi(aw[i]), bf16_hi(bw[i]), c[2 * i + 1], s[2 * i + 1], y1h, y2h);
+                ya[i] = pack_bf16x2(y1l, y1h);
+                yb[i] = pack_bf16x2(y2l, y2h);
+            }
+            __nv_bfloat16 *dst = dst0 + g * head_stride;
+            *reinterpret_cast<uint4 *>(dst + k0) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+            *reinterpret_cast<uint4 *>(dst + k0 + half) = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+        }
+    } else {
+        const int d0 = r + (it - n_rot) * 8;
+        for (int g = 0; g < P.Hkv; ++g)
+            *reinterpret_cast<uint4 *>(dst0 + g * head_stride + d0) =
+                *reinterpret_cast<const uint4 *>(src + g * kHeadDim + d0);
+    }
+}
+
+// ---------------------------------------------------------------- attention
+
+constexpr int kBM = 128;                  // query rows per tile
+constexpr int kBN = 128;                  // keys per tile
+constexpr int kSlotBytes = 16384;         // ring slot: 128 keys x 64 dims (K) or 32 keys x 256 (V)
+constexpr int kSlots = 8;
+constexpr int kQBytes = 4 * kSlotBytes;   // 128 rows x 256 dims, as 4 chunks of 64 dims
+constexpr int kAttnThreads = 256;
+constexpr int kSoftmaxWarp0 = 4;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 0, kColS = 256;
+
+// barriers
+constexpr int kBarQFull = 0;
+constexpr int kBarQReady = 1;
+constexpr int kBarSlotFull = 2;                 // kSlots of them
+constexpr int kBarSlotEmpty = 2 + kSlots;       // kSlots of them
+constexpr int kBarSFull = 2 + 2 * kSlots;       // 2
+constexpr int kBarPReady = 4 + 2 * kSlots;      // 2
+constexpr int kBarODone = 6 + 2 * kSlots;
+constexpr int kBarMmaDrain = 7 + 2 * kSlots;
+constexpr int kNumBars = 8 + 2 * kSlots;
+
+constexpr int kAttnSmemBytes = 1024 + kQBytes + kSlots * kSlotBytes + 256;
+
+constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, 0, 0);        // Q, K both K-major
+constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kHeadDim, 0, 1);   // V is N(=dim)-major
+
+// Byte offset of 16-byte granule `gran` (0..31 across the 256 dims) of row
+// `row` inside a tile stored as 4 chunks of [rows][64 dims] with the 128-byte
+// TMA swizzle (granule index XOR row mod 8 inside each 1024-byte atom).
+__device__ __forceinline__ uint32_t sw128_offset(int row, int gran) {
+    return static_cast<uint32_t>((gran >> 3) * kSlotBytes + row * 128 +
+                                 (((gran & 7) ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ void named_bar(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_kv_k,
+                        const __grid_constant__ CUtensorMap tm_kv_v,
+                        const __grid_constant__ CUtensorMap tm_krot,
+                        const __grid_constant__ CUtensorMap tm_out,
+                        const __grid_constant__ PrefillParams P) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *qbuf = smem;
+    uint8_t *ring = smem + kQBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + kSlots * kSlotBytes);
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_flag;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = P.G, tq = kBM / G;
+    const int units = P.Hkv * P.B;
+    const int qtile = P.n_qtiles - 1 - static_cast<int>(blockIdx.x) / units;  // longest first
+    const int rem = static_cast<int>(blockIdx.x) % units;
+    const int g = rem % P.Hkv, b = rem / P.Hkv;
+    const int t0 = qtile * tq;
+    const int t_end = (t0 + tq < P.T) ? t0 + tq : P.T;  // exclusive
+    const int kv_lo = (P.kind == kLayerFull) ? 0 : (t0 - P.window + 1 > 0 ? t0 - P.window + 1 : 0);
+    const int kv_hi = t_end;
+    const int ntiles = (kv_hi - kv_lo + kBN - 1) / kBN;
+
+    if (tid == 0) {
+        for (int i = 0; i < kNumBars; ++i) {
+            uint32_t count = 1;
+            if (i == kBarQReady || i == kBarPReady || i == kBarPReady + 1) count = 128;
+            mbar_init(&bars[i], count);
+        }
+        fence_mbar_init();
+        abort_flag = 0;
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_base_sh, kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_kv_k);
+        tma_prefetch_desc(&tm_kv_v);
+        if (P.rot_w > 0) tma_prefetch_desc(&tm_krot);
+        tma_prefetch_desc(&tm_out);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        int sc = 0;  // ring slots filled so far
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&bars[kBarQFull], kQBytes);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                tma_load_4d(qbuf + c * kSlotBytes, &tm_q, &bars[kBarQFull], c * 64, g * G, t0, b);
+            bool ok = true;
+            auto next_slot = [&](int &slot) -> bool {
+                slot = sc % kSlots;
+                if (sc >= kSlots &&
+                    !mbar_wait(&bars[kBarSlotEmpty + slot], ((sc / kSlots) - 1) & 1, &abort_flag,
+                               P.status))
+                    return false;
+                mbar_arrive_expect_tx(&bars[kBarSlotFull + slot], kSlotBytes);
+                return true;
+            };
+            auto load_k = [&](int j) -> bool {
+                const int key0 = kv_lo + j * kBN;
+                for (int c = 0; c < 4; ++c) {
+                    int slot;
+                    if (!next_slot(slot)) return false;
+                    uint8_t *dst = ring + slot * kSlotBytes;
+                    if (c * 64 < P.rot_w)
+                        tma_load_3d(dst, &tm_krot, &bars[kBarSlotFull + slot], c * 64, key0,
+                                    b * P.Hkv + g);
+                    else
+                        tma_load_4d(dst, &tm_kv_k, &bars[kBarSlotFull + slot], c * 64, P.H + g,
+                                    key0, b);
+                    ++sc;
+                }
+                return true;
+            };
+            auto load_v = [&](int j) -> bool {
+                const int key0 = kv_lo + j * kBN;
+                for (int vs = 0; vs < 4; ++vs) {
+                    int slot;
+                    if (!next_slot(slot)) return false;
+                    uint8_t *dst = ring + slot * kSlotBytes;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        tma_load_4d(dst + c * (kSlotBytes / 4), &tm_kv_v,
+                                    &bars[kBarSlotFull + slot], c * 64, P.H + P.Hkv + g,
+                                    key0 + vs * 32, b);
+                    ++sc;
+                }
+                return true;
+            };
+            ok = load_k(0);
+            if (ok && ntiles > 1) ok = load_k(1);
+            for (int j = 0; ok && j < ntiles; ++j) {
+                ok = load_v(j);
+                if (ok && j + 2 < ntiles) ok = load_k(j + 2);
+            }
+        }
+        __syncwarp();
+        tc_fence_before();
+        __syncthreads();
+        // after an abort, copies in flight must land before shared memory is released
+        if (lane == 0 && abort_flag) {
+            mbar_wait_plain(&bars[kBarQFull], 0);
+            const int first = sc > kSlots ? sc - kSlots : 0;
+            for (int s = first; s < sc; ++s)
+                mbar_wait_plain(&bars[kBarSlotFull + (s % kSlots)], (s / kSlots) & 1);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int sc = 0;
+            const uint32_t q_addr = smem_u32(qbuf);
+            const uint32_t ring_addr = smem_u32(ring);
+            bool ok = mbar_wait(&bars[kBarQReady], 0, &abort_flag, P.status);
+            tc_fence_after();
+            auto mma_qk = [&](int j) -> bool {
+                const uint32_t d = tmem + kColS + (j & 1) * kBN;
+                for (int c = 0; c < 4; ++c) {
+                    const int slot = sc % kSlots;
+                    if (!mbar_wait(&bars[kBarSlotFull + slot], (sc / kSlots) & 1, &abort_flag,
+                                   P.status))
+                        return false;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = smem_desc_sw128(q_addr + c * kSlotBytes + kk * 32, 16, 1024);
+                        const uint64_t bd = smem_desc_sw128(ring_addr + slot * kSlotBytes + kk * 32, 16, 1024);
+                        mma_ss(d, ad, bd, kIdescQK, (c | kk) != 0);
+                    }
+                    tc_commit(&bars[kBarSlotEmpty + slot]);
+                    ++sc;
+                }
+                tc_commit(&bars[kBarSFull + (j & 1)]);
+                return true;
+            };
+            auto mma_pv = [&](int j) -> bool {
+                const uint32_t pcol = tmem + kColS + (j & 1) * kBN;
+                for (int vs = 0; vs < 4; ++vs) {
+                    const int slot = sc % kSlots;
+                    if (!mbar_wait(&bars[kBarSlotFull + slot], (sc / kSlots) & 1, &abort_flag,
+                                   P.status))
+                        return false;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk) {
+                        const int ks = vs * 2 + kk;  // 16-key step within the tile
+                        const uint64_t bd = smem_desc_sw128(ring_addr + slot * kSlotBytes + kk * 2048,
+                                                            kSlotBytes / 4, 1024);
+                        mma_ts(tmem + kColO, pcol + ks * 8, bd, kIdescPV, (j > 0 || ks > 0));
+                    }
+                    tc_commit(&bars[kBarSlotEmpty + slot]);
+                    ++sc;
+                }
+                tc_commit(&bars[kBarODone]);
+                return true;
+            };
+            if (ok) ok = mma_qk(0);
+            if (ok && ntiles > 1) ok = mma_qk(1);
+            for (int j = 0; ok && j < ntiles; ++j) {
+                ok = mbar_wait(&bars[kBarPReady + (j & 1)], (j >> 1) & 1, &abort_flag, P.status);
+                if (!ok) break;
+                tc_fence_after();
+                ok = mma_pv(j);
+                if (ok && j + 2 < ntiles) ok = mma_qk(j + 2);
+            }
+            // every MMA issued so far must finish before TMEM is released
+            tc_commit(&bars[kBarMmaDrain]);
+            mbar_wait_plain(&bars[kBarMmaDrain], 0);
+        }
+        __syncwarp();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    } else if (warp >= kSoftmaxWarp0) {
+        // ------------------------------------------------------ softmax
+        const int row = tid - kSoftmaxWarp0 * 32;  // TMEM lane, query row
+        const int wq = warp - kSoftmaxWarp0;       // lane quarter of this warp
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+        const int tok = t0 + row / G;
+        const int head = g * G + row % G;
+        const bool valid = tok < P.T;
+        const size_t trow = static_cast<size_t>(b) * P.T + (valid ? tok : 0);
+        const int p = valid ? P.pos[trow] : 0;
+        const float gate_logit = valid ? P.gate[trow * P.H + head] : 0.f;
+        bool ok = mbar_wait(&bars[kBarQFull], 0, &abort_flag, P.status);
+
+        // rotate this row of Q in place (bf16 in, fp32 math, bf16 out)
+        const int r = P.rope.rot_dim, half = r / 2;
+        if (ok) {
+            for (int k0 = 0; k0 < half; k0 += 8) {
+                uint4 *pa = reinterpret_cast<uint4 *>(qbuf + sw128_offset(row, k0 / 8));
+                uint4 *pb = reinterpret_cast<uint4 *>(qbuf + sw128_offset(row, (k0 + half) / 8));
+                const uint4 a = *pa, bb = *pb;
+                const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+                const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
+                uint32_t ya[4], yb[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float c0, s0, c1, s1, y1l, y2l, y1h, y2h;
+                    rope_cos_sin(p, P.rope.u[k0 + 2 * i], c0, s0);
+                    rope_cos_sin(p, P.rope.u[k0 + 2 * i + 1], c1, s1);
+                    rope_rotate(bf16_lo(aw[i]), bf16_lo(bw[i]), c0, s0, y1l, y2l);
+                    rope_rotate(bf16_hi(aw[i]), bf16_hi(bw[i]), c1, s1, y1h, y2h);
+                    ya[i] = pack_bf16x2(y1l, y1h);
+                    yb[i] = pack_bf16x2(y2l, y2h);
+                }
+                *pa = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+                *pb = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+            }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars[kBarQReady]);
+
+        const int t_last = t_end - 1;
+        float m_run = -INFINITY, l_run = 0.f;
+        for (int j = 0; ok && j < ntiles; ++j) {
+            ok = mbar_wait(&bars[kBarSFull + (j & 1)], (j >> 1) & 1, &abort_flag, P.status);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t sbase = lane_base + kColS + (j & 1) * kBN;
+            uint32_t sv[128];
+            tmem_ld32(sbase + 0, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+            tmem_ld32(sbase + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+            tmem_ld32(sbase + 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[64]));
+            tmem_ld32(sbase + 96, *reinterpret_cast<uint32_t(*)[32]>(&sv[96]));
+            tmem_ld_wait();
+            float x[128];
+#pragma unroll
+            for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sv[c]) * kScaleLog2;
+            const int key0 = kv_lo + j * kBN;
+            const bool need_mask = (key0 + kBN - 1 > t0) ||
+                                   (P.kind == kLayerSliding && t_last - key0 >= P.window);
+            if (need_mask) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    const int key = key0 + c;
+                    const bool vis = key <= tok && (P.kind == kLayerFull || tok - key < P.window);
+                    x[c] = vis ? x[c] : -INFINITY;
+                }
+            }
+            float mx = x[0];
+#pragma unroll
+            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
+            const float m_new = fmaxf(m_run, mx);
+            // Move the reference maximum only when it grew by more than 2^8;
+            // what is already summed is then rescaled.  tcgen05.ld/st are
+            // warp-collective, so the O rescale runs for the whole warp (alpha
+            // is 1 on rows that keep their reference).
+            const bool bump = m_new > m_run + 8.0f;
+            const bool rescale_row = bump && m_run != -INFINITY;
+            const float alpha = rescale_row ? fast_exp2(m_run - m_new) : 1.f;
+            if (bump) {
+                l_run *= alpha;
+                m_run = m_new;
+            }
+            if (j > 0 && __any_sync(0xffffffffu, rescale_row)) {
+                ok = mbar_wait(&bars[kBarODone], (j - 1) & 1, &abort_flag, P.status);
+                if (!ok) break;
+                tc_fence_after();
+                for (int c = 0; c < kHeadDim; c += 32) {
+                    uint32_t ov[32];
+                    tmem_ld32(lane_base + kColO + c, ov);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                    tmem_st32(lane_base + kColO + c, ov);
+                }
+            }
+            const float z = (m_run == -INFINITY) ? 0.f : m_run;
+            uint32_t pk[64];
+            float lsum = 0.f;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                const float p0 = fast_exp2(x[2 * c] - z);
+                const float p1 = fast_exp2(x[2 * c + 1] - z);
+                lsum += p0 + p1;
+                pk[c] = pack_bf16x2(p0, p1);
+            }
+            l_run += lsum;
+            tmem_st32(sbase + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+            tmem_st32(sbase + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&bars[kBarPReady + (j & 1)]);
+        }
+
+        // epilogue: O / l * sigmoid(gate) -> bf16 -> staged in the Q buffer -> TMA store
+        if (ok) ok = mbar_wait(&bars[kBarODone], (ntiles - 1) & 1, &abort_flag, P.status);
+        named_bar(1, 128);
+        const bool all_ok = !abort_flag;
+        if (all_ok) {
+            tc_fence_after();
+            const float scale = valid ? sigmoid_f32(gate_logit) / l_run : 0.f;
+            for (int c = 0; c < kHeadDim; c += 32) {
+                uint32_t ov[32];
+                tmem_ld32(lane_base + kColO + c, ov);
+                tmem_ld_wait();
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(ov[8 * q + 0]) * scale,
+                                      __uint_as_float(ov[8 * q + 1]) * scale);
+                    w.y = pack_bf16x2(__uint_as_float(ov[8 * q + 2]) * scale,
+                                      __uint_as_float(ov[8 * q + 3]) * scale);
+                    w.z = pack_bf16x2(__uint_as_float(ov[8 * q + 4]) * scale,
+                                      __uint_as_float(ov[8 * q + 5]) * scale);
+                    w.w = pack_bf16x2(__uint_as_float(ov[8 * q + 6]) * scale,
+                                      __uint_as_float(ov[8 * q + 7]) * scale);
+                    *reinterpret_cast<uint4 *>(qbuf + sw128_offset(row, c / 8 + q)) = w;
+                }
+            }
+            fence_proxy_async_smem();
+            named_bar(1, 128);
+            if (row == 0) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    tma_store_4d(&tm_out, qbuf + c * kSlotBytes, c * 64, g * G, t0, b);
+                tma_store_commit();
+                tma_store_wait_all();
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+    } else {
+        // warps 2 and 3 have no role yet
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------- launcher
+
+cudaError_t launch_prefill(const CUtensorMap &tm_q, const CUtensorMap &tm_kv_k,
+                           const CUtensorMap &tm_kv_v, const CUtensorMap &tm_krot,
+                           const CUtensorMap &tm_out, const PrefillParams &P,
+                           cudaStream_t stream) {
+    if (P.rot_w > 0) {
+        const int r = P.rope.rot_dim;
+        const long long items = r / 16 + (P.rot_w - r) / 8;
+        const long long threads = static_cast<long long>(P.B) * P.T * items;
+        const long long blocks = (threads + kRopeThreads - 1) / kRopeThreads;
+        prefill_rope_k_kernel<<<static_cast<unsigned>(blocks), kRopeThreads, 0, stream>>>(P);
+        cudaError_t err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+    }
+    cudaError_t err = cudaFuncSetAttribute(prefill_attn_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kAttnSmemBytes);
+    if (err != cudaSuccess) return err;
+    const unsigned grid = static_cast<unsigned>(P.n_qtiles) * P.Hkv * P.B;
+    prefill_attn_kernel<<<grid, kAttnThreads, kAttnSmemBytes, stream>>>(tm_q, tm_kv_k, tm_kv_v,
+                                                                        tm_krot, tm_out, P);
+    return cudaGetLastError();
+}
+
+}  // namespace spark

@@ -1,0 +1,167 @@
+/*
+ * spark_attn.h -- C ABI of the Spark-X2.5 gated GQA attention core on one
+ * GB300 (sm_103a).
+ *
+ * What the library computes (page titles and sections of the sources):
+ *
+ *  Spark-X2.5 architecture (4B / 1.7B), §3 "head-wise output gate", Eq. 1:
+ *      out = ( softmax(Q K^T / sqrt(256)) V ) * sigmoid(gate_logit)
+ *  per query head, the gate being one fp32 scalar per (token, head) that is
+ *  broadcast over the head's 256 dims.  Q, K, V come from the fused
+ *  q_k_v_proj output, laid out per token as Q (H heads) || K (Hkv heads) ||
+ *  V (Hkv heads), 256 bf16 each (same §3: width H*256 + 2*Hkv*256).  Query
+ *  head h reads KV head h / (H/Hkv) (grouped-query attention, §1 table).
+ *
+ *  Same page, §4 "layered RoPE": Q and K are rotated before the product.
+ *  For k < r/2, with r = rot_dim and a = pos * theta^(-2k/r):
+ *      y_k = x_k cos a - x_{k+r/2} sin a,  y_{k+r/2} = x_{k+r/2} cos a + x_k sin a
+ *  dims >= r pass through unchanged (partial RoPE: full_attention layers use
+ *  theta 5e6 and r = 64, sliding_attention layers theta 1e4 and r = 256).
+ *
+ *  Same page, §2 "hybrid attention": full layers are causal (key j visible
+ *  from query i iff j <= i); sliding layers add the window, key j visible
+ *  iff 0 <= i - j < window (512 in both released models; the window
+ *  includes the query itself).
+ *
+ *  Decode follows the KV-cache behaviour the Spark-X2.5-4B hybrid-attention
+ *  explainer (lshu.cn) describes: full layers keep every token, sliding
+ *  layers keep only the latest `window` tokens.  Here a full layer's cache is
+ *  contiguous (token j at slot j) and a sliding layer's cache is a ring of
+ *  `cap` slots (token j at slot j mod cap, cap >= window).  Cached keys are
+ *  stored after RoPE.  A step first writes the new token's rotated key and
+ *  its value into slot(pos), then attends over the visible tokens.
+ *
+ * Numerics: bf16 inputs and outputs, fp32 accumulation.  Rotated Q and K are
+ * rounded to bf16 once (tensor-core operands), softmax probabilities are
+ * rounded to bf16 for the P*V product, the gate multiplies the fp32
+ * normalised output and the result is rounded to bf16 (round to nearest even).
+ * RoPE angles are reduced exactly in fp32 (positions below 2^24).
+ *
+ * Conventions for every entry point:
+ *  - All data pointers are DEVICE pointers of the current CUDA device, 16-byte
+ *    aligned, dense row-major in the stated layout.  The caller owns every
+ *    buffer; the library allocates no device memory and keeps no per-call
+ *    state between calls.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and runs asynchronously; nothing synchronizes.
+ *  - Argument errors are found on the host before anything is enqueued; the
+ *    call then returns the status and leaves every output untouched.
+ *  - Faults found on the device (a position outside the cache, a bounded wait
+ *    that ran out) set bits in the workspace's status word (see
+ *    spark_attn_read_status); the kernels never trap.
+ *  - B == 0 (and T == 0 for prefill) is a valid empty call: SPARK_OK, nothing
+ *    is enqueued.
+ */
+#ifndef SPARK_ATTN_H
+#define SPARK_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPARK_HEAD_DIM 256
+
+typedef enum spark_status {
+    SPARK_OK = 0,
+    SPARK_ERR_NULL = 1,        /* a required pointer is NULL */
+    SPARK_ERR_SHAPE = 2,       /* a size is negative or inconsistent (H % Hkv, window < 1, ...) */
+    SPARK_ERR_UNSUPPORTED = 3, /* valid but not built: H/Hkv not in {1,2,4,8}, rot_dim not a
+                                  multiple of 16, gate_mode other than sigmoid */
+    SPARK_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned (workspace: 256-byte) */
+    SPARK_ERR_CAPACITY = 5,    /* a sliding ring smaller than its window, cap < 1 */
+    SPARK_ERR_WORKSPACE = 6,   /* workspace NULL or smaller than the size query returns */
+    SPARK_ERR_CUDA = 7,        /* a CUDA call failed while enqueuing (no device, launch error) */
+    SPARK_ERR_DEVICE = 8       /* the current device is not an sm_103 GPU */
+} spark_status;
+
+typedef enum spark_layer_kind {
+    SPARK_LAYER_FULL = 0,      /* causal; contiguous decode cache */
+    SPARK_LAYER_SLIDING = 1    /* causal sliding window; ring decode cache */
+} spark_layer_kind;
+
+typedef enum spark_gate_mode {
+    SPARK_GATE_SIGMOID = 0     /* out *= 1 / (1 + exp(-gate_logit)) */
+} spark_gate_mode;
+
+/* Layer-type descriptor (the per-layer fields of the model config). */
+typedef struct spark_layer_desc {
+    int32_t kind;        /* spark_layer_kind */
+    int32_t window;      /* SLIDING: window W >= 1; FULL: ignored */
+    double rope_theta;   /* RoPE base theta > 0 */
+    int32_t rot_dim;     /* rotated dims r: 0 <= r <= 256, multiple of 16 (0 = no RoPE) */
+    int32_t gate_mode;   /* spark_gate_mode */
+} spark_layer_desc;
+
+/* Bits of the device status word in the workspace. */
+#define SPARK_DEVERR_POSITION 0x1u /* a decode position was negative or >= cap (FULL);
+                                      that sequence was skipped */
+#define SPARK_DEVERR_TIMEOUT 0x2u  /* a bounded on-chip wait ran out; results are invalid */
+
+/*
+ * Prefill: attention of T new tokens per sequence over themselves.
+ *
+ *   qkv   bf16 [B, T, (H + 2*Hkv) * 256]   fused projection, per token Q||K||V
+ *   gate  fp32 [B, T, H]                   gate logits
+ *   pos   int32 [B, T]                     RoPE positions, 0 <= pos < 2^24
+ *   out   bf16 [B, T, H * 256]             gated output, head h at columns h*256..
+ *   workspace  >= spark_attn_prefill_workspace_size(...) bytes, 256-byte
+ *              aligned, zeroed once before first use (see spark_attn_read_status)
+ *
+ * The mask is applied on the token index t inside the sequence (query t sees
+ * keys t' <= t, and t - t' < window on SLIDING layers); RoPE uses pos.
+ * Returns 0 from the size query for invalid arguments.
+ */
+size_t spark_attn_prefill_workspace_size(int B, int T, int H, int Hkv,
+                                         const spark_layer_desc *desc);
+
+spark_status spark_attn_prefill(const void *qkv, const float *gate, const int32_t *pos,
+                                const spark_layer_desc *desc, int B, int T, int H, int Hkv,
+                                void *out, void *workspace, size_t workspace_bytes,
+                                void *stream);
+
+/*
+ * Decode: one new token per sequence.
+ *
+ *   qkv      bf16 [B, (H + 2*Hkv) * 256]   the new token's fused projection
+ *   gate     fp32 [B, H]
+ *   pos      int32 [B]   position of the new token = tokens already cached
+ *   k_cache, v_cache  bf16 [B, Hkv, cap, 256], updated in place.
+ *            FULL: token j at slot j, needs pos < cap (else the sequence is
+ *            skipped and SPARK_DEVERR_POSITION is set).
+ *            SLIDING: ring, token j at slot j mod cap, needs cap >= window.
+ *   out      bf16 [B, H * 256]
+ *   workspace >= spark_attn_decode_workspace_size(...) bytes (split-KV
+ *            partial softmax states), 256-byte aligned, zeroed once before
+ *            first use.
+ * Returns 0 from the size query for invalid arguments.
+ */
+size_t spark_attn_decode_workspace_size(int B, int H, int Hkv, int64_t cap,
+                                        const spark_layer_desc *desc);
+
+spark_status spark_attn_decode(const void *qkv, const float *gate, const int32_t *pos,
+                               void *k_cache, void *v_cache, int64_t cap,
+                               const spark_layer_desc *desc, int B, int H, int Hkv,
+                               void *out, void *workspace, size_t workspace_bytes,
+                               void *stream);
+
+/*
+ * Copies the sticky device status word out of a workspace (synchronizes on
+ * `stream`).  If `clear` is non-zero the word is reset to 0 afterwards.
+ */
+spark_status spark_attn_read_status(void *workspace, uint32_t *status_out, int clear,
+                                    void *stream);
+
+/* Static description of a status code (never NULL). */
+const char *spark_status_str(spark_status status);
+
+/* Library build version, "major.minor.patch". */
+const char *spark_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARK_ATTN_H */
