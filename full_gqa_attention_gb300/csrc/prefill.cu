@@ -102,7 +102,8 @@ constexpr int kBarSFull = 2 + 2 * kSlots;       // 2
 constexpr int kBarPReady = 4 + 2 * kSlots;      // 2
 constexpr int kBarODone = 6 + 2 * kSlots;
 constexpr int kBarMmaDrain = 7 + 2 * kSlots;
-constexpr int kNumBars = 8 + 2 * kSlots;
+constexpr int kBarOFinal = 8 + 2 * kSlots;      // every P*V done (one phase per CTA)
+constexpr int kNumBars = 9 + 2 * kSlots;
 
 constexpr int kAttnSmemBytes = 1024 + kQBytes + kSlots * kSlotBytes + 256;
 
@@ -296,8 +297,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
                 ok = mma_pv(j);
-                if (ok && j + 2 < ntiles) ok = mma_qk(j + 2);
+                if (ok && j + 2 < ntiles) {
+                    // QK^T of tile j+2 overwrites the score buffer whose first
+                    // half holds P_j.  tcgen05.mma keeps issue order only among
+                    // products into the same accumulator, so wait until P*V of
+                    // tile j (accumulator O) has finished reading P_j.
+                    ok = mbar_wait(&bars[kBarODone], j & 1, &abort_flag, P.status);
+                    if (ok) {
+                        tc_fence_after();
+                        ok = mma_qk(j + 2);
+                    }
+                }
             }
+            // The epilogue waits on a barrier of its own: a parity wait on
+            // kBarODone could be two phases behind when the last softmax tile
+            // finishes before P*V of the tile before it.
+            if (ok) tc_commit(&bars[kBarOFinal]);
             // every MMA issued so far must finish before TMEM is released
             tc_commit(&bars[kBarMmaDrain]);
             mbar_wait_plain(&bars[kBarMmaDrain], 0);
@@ -422,7 +437,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
 
         // epilogue: O / l * sigmoid(gate) -> bf16 -> staged in the Q buffer -> TMA store
-        if (ok) ok = mbar_wait(&bars[kBarODone], (ntiles - 1) & 1, &abort_flag, P.status);
+        if (ok) ok = mbar_wait(&bars[kBarOFinal], 0, &abort_flag, P.status);
         named_bar(1, 128);
         const bool all_ok = !abort_flag;
         if (all_ok) {

@@ -1,0 +1,182 @@
+"""GPU parity of one decode step against the fp64 oracle (through the C ABI).
+
+Output: max-abs <= 2e-2 and rel-L2 <= 1e-2.  Cache update: the slot of the
+new position is rewritten (value bit-exact, unrotated key dims bit-exact,
+rotated key dims within one bf16 ulp of the rounded fp64 rotation: the GPU
+rotates in fp32), every other slot is untouched bit for bit.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import full_gqa_attention_gb300 as fga
+import oracle
+import workloads as wl
+from parity import bf16_ulp_diff, check_close, f64_to_bf16_bits
+
+pytestmark = pytest.mark.gpu
+
+FULL, SLIDING = wl.FULL, wl.SLIDING
+
+
+def run_case(cuda, layer, H, Hkv, cap, positions, seed, check_cache=True):
+    B = len(positions)
+    case = wl.DecodeCase("t", B=B, H=H, Hkv=Hkv, layer=layer, seed=seed, cap=cap,
+                         len_lo=0, len_hi=0)
+    step = wl.make_decode_step_inputs(case)
+    pos = torch.tensor(positions, dtype=torch.int32)
+    kc = wl.fill_cache_(torch.empty((B, Hkv, cap, 256), dtype=torch.bfloat16), seed + 11)
+    vc = wl.fill_cache_(torch.empty_like(kc), seed + 12)
+    kd, vd = kc.to(cuda), vc.to(cuda)
+    ws = fga.new_workspace(fga.spark_attn_decode_workspace_size(B, H, Hkv, cap, layer))
+    out = fga.spark_attn_decode(step["qkv"].to(cuda), step["gate"].to(cuda), pos.to(cuda), kd,
+                                vd, layer, workspace=ws)
+    torch.cuda.synchronize()
+    assert fga.spark_attn_read_status(ws) == 0
+    want, k_new, v_new = oracle.decode(wl.bf16_bits(step["qkv"]), step["gate"].numpy(),
+                                       pos.numpy(), wl.bf16_bits(kc), wl.bf16_bits(vc),
+                                       layer.kind, layer.window, layer.theta, layer.rot_dim, H,
+                                       Hkv)
+    check_close(out, want, f"decode kind={layer.kind} G={H // Hkv} cap={cap} pos={positions}")
+    if check_cache:
+        kb, vb = wl.bf16_bits(kd), wl.bf16_bits(vd)
+        k0, v0 = wl.bf16_bits(kc), wl.bf16_bits(vc)
+        for b, p in enumerate(positions):
+            slot = p if layer.kind == FULL else p % cap
+            kb_slot, vb_slot = kb[b, :, slot].copy(), vb[b, :, slot].copy()
+            assert np.array_equal(vb_slot, f64_to_bf16_bits(v_new[b])), "value slot"
+            r = layer.rot_dim
+            want_k = f64_to_bf16_bits(k_new[b])
+            assert np.array_equal(kb_slot[:, r:], want_k[:, r:]), "unrotated key dims"
+            assert bf16_ulp_diff(kb_slot[:, :r], want_k[:, :r]).max(initial=0) <= 1
+            kb[b, :, slot] = k0[b, :, slot]
+            vb[b, :, slot] = v0[b, :, slot]
+        assert np.array_equal(kb, k0) and np.array_equal(vb, v0), "other cache slots changed"
+    return out
+
+
+@pytest.mark.parametrize("positions", [[0, 1, 63, 64], [65, 1000, 4095, 2047]])
+def test_full_layer_4b(cuda, positions):
+    run_case(cuda, wl.FULL_LAYER, 16, 4, 4096, positions, seed=1)
+
+
+@pytest.mark.parametrize("positions", [[0, 1, 300, 510], [511, 512, 513, 1023],
+                                       [1024, 5000, 131071, 1048575]])
+def test_sliding_ring_512(cuda, positions):
+    run_case(cuda, wl.SLIDING_LAYER, 16, 4, 512, positions, seed=2)
+
+
+def test_ring_larger_than_window(cuda):
+    run_case(cuda, wl.SLIDING_LAYER, 16, 4, 600, [100, 599, 600, 601, 1799, 2000], seed=3)
+
+
+@pytest.mark.parametrize("H,Hkv", [(8, 8), (8, 4), (16, 2), (8, 2)])
+def test_group_sizes(cuda, H, Hkv):
+    run_case(cuda, wl.FULL_LAYER, H, Hkv, 1500, [7, 640, 1499], seed=4)
+    run_case(cuda, wl.SLIDING_LAYER, H, Hkv, 512, [7, 700], seed=5)
+
+
+@pytest.mark.parametrize("rot", [0, 16, 128])
+def test_rotary_widths(cuda, rot):
+    layer = wl.Layer(kind=FULL, window=0, theta=5e6, rot_dim=rot)
+    run_case(cuda, layer, 16, 4, 2100, [1, 2049, 2099], seed=6)
+
+
+def test_small_windows(cuda):
+    for W in (1, 2, 100):
+        layer = wl.Layer(kind=SLIDING, window=W, theta=1e4, rot_dim=256)
+        run_case(cuda, layer, 8, 2, max(W, 128), [0, 1, W, 3 * W + 5], seed=7 + W)
+
+
+def test_split_count_invariance(cuda):
+    """The same tokens through differently split caches give one answer."""
+    outs = []
+    for cap in (1100, 5000, 70000):
+        torch.manual_seed(0)
+        B, H, Hkv = 1, 16, 4
+        case = wl.DecodeCase("t", B=B, H=H, Hkv=Hkv, layer=wl.FULL_LAYER, seed=8, cap=cap,
+                             len_lo=0, len_hi=0)
+        step = wl.make_decode_step_inputs(case)
+        pos = torch.tensor([1050], dtype=torch.int32)
+        kc = torch.zeros((B, Hkv, cap, 256), dtype=torch.bfloat16)
+        vc = torch.zeros_like(kc)
+        base = wl.fill_cache_(torch.empty((B, Hkv, 1100, 256), dtype=torch.bfloat16), 9)
+        kc[:, :, :1100] = base
+        vc[:, :, :1100] = base.flip(-1)
+        out = fga.spark_attn_decode(step["qkv"].to(cuda), step["gate"].to(cuda), pos.to(cuda),
+                                    kc.to(cuda), vc.to(cuda), wl.FULL_LAYER)
+        outs.append(out.float().cpu())
+    for o in outs[1:]:
+        assert torch.allclose(o, outs[0], atol=8e-3, rtol=0)
+
+
+def test_bad_position_is_flagged(cuda):
+    """A full-layer position at or past the cache end is skipped and flagged;
+    the other sequences are still computed."""
+    layer = wl.FULL_LAYER
+    B, H, Hkv, cap = 2, 16, 4, 256
+    case = wl.DecodeCase("t", B=B, H=H, Hkv=Hkv, layer=layer, seed=10, cap=cap, len_lo=0,
+                         len_hi=0)
+    step = wl.make_decode_step_inputs(case)
+    kc = wl.fill_cache_(torch.empty((B, Hkv, cap, 256), dtype=torch.bfloat16), 3).to(cuda)
+    vc = wl.fill_cache_(torch.empty((B, Hkv, cap, 256), dtype=torch.bfloat16), 4).to(cuda)
+    pos = torch.tensor([100, 256], dtype=torch.int32, device=cuda)
+    out = torch.full((B, H * 256), 7.0, dtype=torch.bfloat16, device=cuda)
+    ws = fga.new_workspace(fga.spark_attn_decode_workspace_size(B, H, Hkv, cap, layer))
+    fga.spark_attn_decode(step["qkv"].to(cuda), step["gate"].to(cuda), pos, kc, vc, layer,
+                          out=out, workspace=ws)
+    status = fga.spark_attn_read_status(ws, clear=True)
+    assert status == fga.SPARK_DEVERR_POSITION
+    assert torch.all(out[1] == 7.0), "skipped sequence must be left untouched"
+    assert fga.spark_attn_read_status(ws) == 0
+
+
+def _full_size(cuda, dcase, sample_b):
+    """Full-size decode; the oracle checks the sampled sequences."""
+    step = wl.make_decode_step_inputs(dcase)
+    B, H, Hkv, cap = dcase.B, dcase.H, dcase.Hkv, dcase.cap
+    kd = torch.empty((B, Hkv, cap, 256), dtype=torch.bfloat16, device=cuda)
+    vd = torch.empty_like(kd)
+    wl.fill_cache_(kd, dcase.seed + 100)
+    wl.fill_cache_(vd, dcase.seed + 200)
+    k_before = {b: kd[b].cpu() for b in sample_b}
+    v_before = {b: vd[b].cpu() for b in sample_b}
+    out = fga.spark_attn_decode(step["qkv"].to(cuda), step["gate"].to(cuda),
+                                step["pos"].to(cuda), kd, vd, dcase.layer)
+    torch.cuda.synchronize()
+    L = dcase.layer
+    for b in sample_b:
+        want, _, _ = oracle.decode(wl.bf16_bits(step["qkv"][b:b + 1]),
+                                   step["gate"][b:b + 1].numpy(), step["pos"][b:b + 1].numpy(),
+                                   wl.bf16_bits(k_before[b][None]),
+                                   wl.bf16_bits(v_before[b][None]), L.kind, L.window, L.theta,
+                                   L.rot_dim, H, Hkv)
+        check_close(out[b:b + 1], want, f"{dcase.name} b={b} pos={int(step['pos'][b])}")
+    del kd, vd
+    torch.cuda.empty_cache()
+
+
+def test_batched_decode_full_size(cuda):
+    d = wl.DECODE_FULL_4B_B64
+    lengths = wl.make_decode_lengths(d)
+    sample = sorted({int(torch.argmin(lengths)), int(torch.argmax(lengths)), 17})
+    _full_size(cuda, d, sample)
+    _full_size(cuda, wl.DECODE_SLIDING_4B_B64, list(range(0, 64, 9)))
+
+
+def test_million_token_decode(cuda):
+    _full_size(cuda, wl.DECODE_FULL_4B_1M, [0])
+    _full_size(cuda, wl.DECODE_SLIDING_4B_1M, [0])
+
+
+def test_empty_batch(cuda):
+    layer = wl.SLIDING_LAYER
+    e = torch.empty((0, 24 * 256), dtype=torch.bfloat16, device=cuda)
+    out = fga.spark_attn_decode(e, torch.empty((0, 16), device=cuda),
+                                torch.empty((0,), dtype=torch.int32, device=cuda),
+                                torch.empty((0, 4, 512, 256), dtype=torch.bfloat16, device=cuda),
+                                torch.empty((0, 4, 512, 256), dtype=torch.bfloat16, device=cuda),
+                                layer)
+    assert out.shape == (0, 16 * 256)
