@@ -1,0 +1,553 @@
+"""Benchmark of the Spark-X2.5 attention core on GB300.
+
+One step is one pass of the whole hot path over one batch of synthetic input:
+  * prefill of a 4B-shaped full_attention layer, B=2, T=8192, H=16, Hkv=4
+    (causal, RoPE theta 5e6 on 64 dims, sigmoid gate): 1.0996 TFLOP;
+  * one 1M-context decode step of all 36 attention cores of the 4B model in
+    layer order (9 full layers with 1,048,575 cached tokens each, 27 sliding
+    layers with full 512-slot rings): 38.71 GB of KV read.
+The JSON line's value is the prefill throughput (TFLOP/s); the decode KV-read
+bandwidth is reported beside it.  Inputs are seeded synthetic tensors of the
+model's shapes (no dataset or weights exist for this path).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {ours,reference}]
+                  [--only {all,prefill,decode}] [--decode-layers L]
+
+Under torchrun every rank runs its own replica (the attention core needs no
+exchange between GPUs); value is the work of all ranks over the slowest rank.
+--impl reference times the fp64 CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+PREFILL = wl.PREFILL_FULL_4B_B2_T8192
+DECODE_FULL = wl.DECODE_FULL_4B_1M
+DECODE_SLIDING = wl.DECODE_SLIDING_4B_1M
+METRIC = "prefill attn TFLOP/s & % bf16 peak; decode KV-read GB/s & % HBM peak (1 GB300)"
+KV_BYTES_PER_TOKEN = 2 * 4 * 256 * 2  # K and V, 4 KV heads, 256 dims, bf16
+
+
+def visible_pairs(T: int, kind: int, window: int) -> int:
+    """Sum over queries of the number of visible keys (mask definition)."""
+    if kind == wl.FULL:
+        return T * (T + 1) // 2
+    W = window
+    if T <= W:
+        return T * (T + 1) // 2
+    return W * (W + 1) // 2 + (T - W) * W
+
+
+def prefill_flops(case) -> float:
+    return 4.0 * 256 * case.B * case.H * visible_pairs(case.T, case.layer.kind,
+                                                        case.layer.window)
+
+
+def decode_layers(n_layers: int):
+    return list(wl.LAYER_TYPES_4B[:n_layers])
+
+
+def decode_kv_bytes(layers) -> tuple[int, int]:
+    """(bytes of all layers, bytes of one full layer) of visible K/V per step."""
+    p = DECODE_FULL.len_hi
+    full = (p + 1) * KV_BYTES_PER_TOKEN
+    sliding = min(p + 1, wl.SLIDING_LAYER.window) * KV_BYTES_PER_TOKEN
+    total = sum(full if l.kind == wl.FULL else sliding for l in layers)
+    return total, full
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+    return rank, world, local
+
+
+def dist_barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def dist_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_sum(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local):
+    import torch
+    import full_gqa_attention_gb300 as fga
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    hbm_peak, bf16_peak, bf16_sust, peak_src = load_peaks()
+    do_prefill = args.only in ("all", "prefill")
+    do_decode = args.only in ("all", "decode")
+    layers = decode_layers(args.decode_layers) if do_decode else []
+
+    # ---- prefill inputs (resident) and their pinned host copies (for e2e)
+    pre = None
+    if do_prefill:
+        x = wl.make_prefill_inputs(PREFILL)
+        pre = {
+            "host": {k: v.pin_memory() for k, v in x.items()},
+            "dev": {k: v.to(dev) for k, v in x.items()},
+        }
+        c = PREFILL
+        pre["out"] = torch.empty((c.B, c.T, c.H * 256), dtype=torch.bfloat16, device=dev)
+        pre["host_out"] = torch.empty_like(pre["out"], device="cpu").pin_memory()
+        pre["ws"] = fga.new_workspace(fga.spark_attn_prefill_workspace_size(
+            c.B, c.T, c.H, c.Hkv, c.layer), dev)
+
+    # ---- decode state: one cache per layer, new-token inputs per layer
+    dec = []
+    for i, layer in enumerate(layers):
+        case = DECODE_FULL if layer.kind == wl.FULL else DECODE_SLIDING
+        step = wl.make_decode_step_inputs(wl.scaled(case, seed=case.seed + 7 * i))
+        kc = torch.empty((case.B, case.Hkv, case.cap, 256), dtype=torch.bfloat16, device=dev)
+        vc = torch.empty_like(kc)
+        g = torch.Generator(dev).manual_seed(1000 + i)
+        kc.normal_(generator=g)
+        vc.normal_(generator=g)
+        dec.append({
+            "case": case, "layer": layer, "k": kc, "v": vc,
+            "host": {k: v.pin_memory() for k, v in step.items()},
+            "dev": {k: v.to(dev) for k, v in step.items()},
+            "out": torch.empty((case.B, case.H * 256), dtype=torch.bfloat16, device=dev),
+            "host_out": torch.empty((case.B, case.H * 256), dtype=torch.bfloat16).pin_memory(),
+            "ws": fga.new_workspace(fga.spark_attn_decode_workspace_size(
+                case.B, case.H, case.Hkv, case.cap, layer), dev),
+        })
+    torch.cuda.synchronize()
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def step(timing=None):
+        if pre is not None:
+            d = pre["dev"]
+            if timing is not None:
+                timing["p0"].append(ev()); timing["p0"][-1].record(stream)
+            fga.spark_attn_prefill(d["qkv"], d["gate"], d["pos"], PREFILL.layer,
+                                   out=pre["out"], workspace=pre["ws"], stream=stream)
+            if timing is not None:
+                timing["p1"].append(ev()); timing["p1"][-1].record(stream)
+        if dec:
+            if timing is not None:
+                timing["d0"].append(ev()); timing["d0"][-1].record(stream)
+            for L in dec:
+                d = L["dev"]
+                full = L["layer"].kind == wl.FULL
+                if timing is not None and full:
+                    e = ev(); e.record(stream); timing["f0"].append(e)
+                fga.spark_attn_decode(d["qkv"], d["gate"], d["pos"], L["k"], L["v"], L["layer"],
+                                      out=L["out"], workspace=L["ws"], stream=stream)
+                if timing is not None and full:
+                    e = ev(); e.record(stream); timing["f1"].append(e)
+            if timing is not None:
+                timing["d1"].append(ev()); timing["d1"][-1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    timing = {k: [] for k in ("p0", "p1", "d0", "d1", "f0", "f1")}
+    start, stop = ev(), ev()
+    with ClockSampler(local) as clocks:
+        dist_barrier(world)
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(args.steps):
+            step(timing)
+        stop.record(stream)
+        torch.cuda.synchronize()
+        dist_barrier(world)
+    total_ms = start.elapsed_time(stop) / args.steps
+
+    def mean_ms(a, b):
+        ts = [x.elapsed_time(y) for x, y in zip(timing[a], timing[b])]
+        return sum(ts) / len(ts) if ts else None
+
+    prefill_ms = mean_ms("p0", "p1")
+    decode_ms = mean_ms("d0", "d1")
+    full_call_ms = mean_ms("f0", "f1")
+
+    # ---- end to end through the public API with host buffers
+    h2d = d2h = 0
+    if pre is not None:
+        h2d += sum(t.numel() * t.element_size() for t in pre["host"].values())
+        d2h += pre["host_out"].numel() * pre["host_out"].element_size()
+    for L in dec:
+        h2d += sum(t.numel() * t.element_size() for t in L["host"].values())
+        d2h += L["host_out"].numel() * L["host_out"].element_size()
+
+    def e2e_step(timing):
+        if pre is not None:
+            d, h = pre["dev"], pre["host"]
+            timing["p0"].append(ev()); timing["p0"][-1].record(stream)
+            for k in d:
+                d[k].copy_(h[k], non_blocking=True)
+            fga.spark_attn_prefill(d["qkv"], d["gate"], d["pos"], PREFILL.layer,
+                                   out=pre["out"], workspace=pre["ws"], stream=stream)
+            pre["host_out"].copy_(pre["out"], non_blocking=True)
+            timing["p1"].append(ev()); timing["p1"][-1].record(stream)
+        if dec:
+            timing["d0"].append(ev()); timing["d0"][-1].record(stream)
+            for L in dec:
+                d, h = L["dev"], L["host"]
+                for k in d:
+                    d[k].copy_(h[k], non_blocking=True)
+                fga.spark_attn_decode(d["qkv"], d["gate"], d["pos"], L["k"], L["v"],
+                                      L["layer"], out=L["out"], workspace=L["ws"],
+                                      stream=stream)
+                L["host_out"].copy_(L["out"], non_blocking=True)
+            timing["d1"].append(ev()); timing["d1"][-1].record(stream)
+
+    e2e_t = {k: [] for k in ("p0", "p1", "d0", "d1")}
+    e2e_step({k: [] for k in e2e_t})
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    for _ in range(args.steps):
+        e2e_step(e2e_t)
+    torch.cuda.synchronize()
+    dist_barrier(world)
+
+    def mean_e2e(a, b):
+        ts = [x.elapsed_time(y) for x, y in zip(e2e_t[a], e2e_t[b])]
+        return sum(ts) / len(ts) if ts else 0.0
+
+    e2e_prefill_ms = mean_e2e("p0", "p1")
+    e2e_decode_ms = mean_e2e("d0", "d1")
+
+    # device status words must be clean
+    status = 0
+    if pre is not None:
+        status |= fga.spark_attn_read_status(pre["ws"])
+    for L in dec:
+        status |= fga.spark_attn_read_status(L["ws"])
+
+    # ---- aggregate over ranks (replicas: work adds up, time is the slowest rank)
+    total_ms_max = dist_max(total_ms, world)
+    pf = prefill_flops(PREFILL) if pre is not None else 0.0
+    kv_total, kv_full = decode_kv_bytes(layers)
+    n_full = sum(1 for l in layers if l.kind == wl.FULL)
+    prefill_ms_max = dist_max(prefill_ms or 0.0, world)
+    decode_ms_max = dist_max(decode_ms or 0.0, world)
+    full_ms_max = dist_max(full_call_ms or 0.0, world)
+    e2e_prefill_max = dist_max(e2e_prefill_ms, world)
+    e2e_decode_max = dist_max(e2e_decode_ms, world)
+    status = int(dist_max(float(status), world))
+    launches = args.steps * ((2 if pre is not None else 0) + 2 * len(dec))
+    launches_all = int(dist_sum(float(launches), world))
+    if rank != 0:
+        return None
+
+    prefill_tflops = world * pf / (prefill_ms_max * 1e9) if pre is not None else None
+    decode_gbs = world * kv_total / (decode_ms_max * 1e6) if dec else None
+    full_gbs = kv_full / (full_ms_max * 1e6) if n_full else None
+    e2e_prefill_tflops = world * pf / (e2e_prefill_max * 1e9) if pre is not None else None
+    e2e_decode_gbs = world * kv_total / (e2e_decode_max * 1e6) if dec else None
+
+    if pre is not None:
+        value, unit = prefill_tflops, "TFLOP/s"
+        e2e_value = e2e_prefill_tflops
+    else:
+        value, unit = decode_gbs, "GB/s"
+        e2e_value = e2e_decode_gbs
+
+    rooflines = []
+    if dec and n_full:
+        rooflines.append({
+            "kernel": "decode_split_kernel (+ decode_merge_kernel in the timed call)",
+            "bound": "hbm", "achieved": full_gbs, "peak": hbm_peak, "unit": "GB/s",
+            "frac": full_gbs / hbm_peak,
+            "traffic": TRAFFIC.get("decode_split_kernel"),
+            "algorithmic_per_launch": kv_full,
+            "peak_source": f"{peak_src} hbm_gbs (copy)"})
+    if pre is not None:
+        achieved = pf / (prefill_ms_max * 1e9)
+        rooflines.append({
+            "kernel": "prefill_attn_kernel (+ prefill_rope_k_kernel in the timed call)",
+            "bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
+            "frac": achieved / bf16_peak,
+            "traffic": TRAFFIC.get("prefill_attn_kernel"),
+            "algorithmic_per_launch": pf,
+            "peak_source": f"{peak_src} bf16_tflops (burst)"})
+    # the dominant kernel of the step by time
+    if dec and pre is not None:
+        dominant = rooflines[0] if (decode_ms_max > prefill_ms_max) else rooflines[1]
+    else:
+        dominant = rooflines[0]
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": unit,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total_ms_max,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded normal activations and KV caches at the 4B model shapes)",
+        "config": {
+            "workload": ("prefill 4B full_attention B=2 T=8192 H=16 Hkv=4 + 1M-context "
+                         "36-layer 4B decode step (9 full, 27 sliding)"
+                         if (pre is not None and dec) else args.only),
+            "prefill": {"B": PREFILL.B, "T": PREFILL.T, "H": PREFILL.H, "Hkv": PREFILL.Hkv,
+                        "kind": "full", "rope_theta": 5e6, "rot_dim": 64} if pre else None,
+            "decode": {"B": 1, "layers": len(dec), "full_layers": n_full,
+                       "cached_tokens": DECODE_FULL.len_hi, "ring_slots": 512} if dec else None,
+            "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (prefill qkv 201 MB; each full-layer cache 4 GiB)",
+        },
+        "prefill": {"ms": prefill_ms_max, "tflops": prefill_tflops,
+                    "frac_bf16_peak": (prefill_tflops / world / bf16_peak) if pre else None,
+                    "flops": pf} if pre is not None else None,
+        "decode": {"ms": decode_ms_max, "kv_gbs": decode_gbs,
+                   "frac_hbm_peak": (decode_gbs / world / hbm_peak) if dec else None,
+                   "kv_bytes": kv_total, "full_layer_call_ms": full_ms_max,
+                   "full_layer_kv_gbs": full_gbs} if dec else None,
+        "roofline": dominant,
+        "rooflines": rooflines,
+        "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "prefill_ms": e2e_prefill_max,
+                "decode_ms": e2e_decode_max, "decode_kv_gbs": e2e_decode_gbs,
+                "api": "full_gqa_attention_gb300.spark_attn_prefill / spark_attn_decode "
+                       "(ctypes -> C ABI), inputs copied from pinned host memory and "
+                       "outputs read back every step"},
+        "gpu_launches": launches_all,
+        "clocks": clocks.summary(),
+        "device_status": status,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args)
+    return line
+
+
+# Per-launch DRAM traffic (read + write bytes) from ncu captures of the
+# current kernels, scaled to one launch of the bench workload; None when the
+# kernels changed since the counters were taken.
+TRAFFIC: dict[str, float | None] = {}
+
+
+# ---------------------------------------------------------------- oracle arm
+
+_ORACLE_INPUTS = {}
+
+
+def oracle_prefill_sample(n_rows: int, seed: int = 0):
+    """Times the fp64 oracle on n_rows query rows of the prefill workload.
+    Returns (seconds, algorithmic flops of those rows, description)."""
+    import numpy as np
+    import oracle
+    c = PREFILL
+    if not _ORACLE_INPUTS:
+        x = wl.make_prefill_inputs(c)
+        _ORACLE_INPUTS.update(x=x, bits=wl.bf16_bits(x["qkv"]))
+    x, bits = _ORACLE_INPUTS["x"], _ORACLE_INPUTS["bits"]
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.integers(0, c.B * c.T, n_rows)).astype(np.int64)
+    L = c.layer
+    t0 = time.perf_counter()
+    oracle.prefill(bits, x["gate"].numpy(), x["pos"].numpy(), L.kind, L.window, L.theta,
+                   L.rot_dim, c.H, c.Hkv, rows=rows)
+    dt = time.perf_counter() - t0
+    flops = 4.0 * 256 * c.H * float(np.sum(rows % c.T + 1))
+    return dt, flops, f"{n_rows} random query rows (all 16 heads) of the B=2 T=8192 prefill"
+
+
+def cpu_threads() -> int:
+    """Threads the OpenMP oracle runs with (its default: the usable cores)."""
+    n = os.environ.get("OMP_NUM_THREADS")
+    if n and n.isdigit():
+        return int(n)
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(args):
+    """The fp64 oracle, as it stands, on a bounded sample (~10-30 s of CPU)."""
+    n = 64
+    while True:
+        dt, flops, desc = oracle_prefill_sample(n)
+        if dt >= 8.0 or n >= 8192:
+            break
+        n = int(n * min(8.0, max(2.0, 10.0 / max(dt, 1e-3))))
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(),
+            "kind": "oracle", "sample": desc + f", {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    rows = 256
+    dt, flops, desc = oracle_prefill_sample(rows, seed=1)
+    # size the sample so the whole run stays within a few minutes
+    per_row = dt / rows
+    rows = max(8, min(4096, int(8.0 / max(per_row, 1e-6))))
+    for _ in range(args.warmup):
+        oracle_prefill_sample(max(8, rows // 8), seed=2)
+    times, total_flops = [], 0.0
+    for k in range(args.steps):
+        dt, flops, desc = oracle_prefill_sample(rows, seed=10 + k)
+        times.append(dt)
+        total_flops += flops
+    secs = sum(times)
+    value = total_flops / secs / 1e12
+    ms_per_step = 1000.0 * secs / args.steps
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded normal activations at the 4B model shapes)",
+        "config": {"workload": "prefill 4B full_attention B=2 T=8192 H=16 Hkv=4 (oracle on a "
+                               "sample of query rows per step)",
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_threads(),
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--only", choices=("all", "prefill", "decode"), default="all")
+    ap.add_argument("--decode-layers", type=int, default=36)
+    ap.add_argument("--decode-cache-tokens", type=int, default=None,
+                    help="cached tokens of each full decode layer (default 1,048,575); "
+                         "smaller values are for profiler captures")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        print("bench.py: warmup raised to 3", file=sys.stderr)
+        args.warmup = 3
+    if args.decode_cache_tokens is not None:
+        global DECODE_FULL
+        n = args.decode_cache_tokens
+        DECODE_FULL = wl.scaled(DECODE_FULL, cap=n + 1, len_lo=n, len_hi=n)
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
