@@ -10,6 +10,7 @@ from ._binding import (  # noqa: F401
     SPARK_GATE_SIGMOID,
     SPARK_LAYER_FULL,
     SPARK_LAYER_SLIDING,
+    SPARK_NOALLOC_SCRATCH_BYTES,
     SPARK_OK,
     SparkError,
     as_desc,
@@ -17,6 +18,7 @@ from ._binding import (  # noqa: F401
     lib,
     new_workspace,
     spark_attn_decode,
+    spark_attn_decode_noalloc,
     spark_attn_decode_workspace_size,
     spark_attn_prefill,
     spark_attn_prefill_workspace_size,

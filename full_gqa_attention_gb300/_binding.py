@@ -29,6 +29,8 @@ SPARK_LAYER_FULL = 0
 SPARK_LAYER_SLIDING = 1
 SPARK_GATE_SIGMOID = 0
 
+SPARK_NOALLOC_SCRATCH_BYTES = 8 << 20
+
 SPARK_DEVERR_POSITION = 0x1
 SPARK_DEVERR_TIMEOUT = 0x2
 
@@ -57,6 +59,8 @@ def _load() -> ctypes.CDLL:
     lib.spark_attn_decode_workspace_size.restype = sz
     lib.spark_attn_decode.argtypes = [P, P, P, P, P, i64, D, i32, i32, i32, P, P, sz, P]
     lib.spark_attn_decode.restype = i32
+    lib.spark_attn_decode_noalloc.argtypes = [P, P, P, P, P, i64, D, i32, i32, i32, P, P, P]
+    lib.spark_attn_decode_noalloc.restype = i32
     lib.spark_attn_read_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), i32, P]
     lib.spark_attn_read_status.restype = i32
     lib.spark_status_str.argtypes = [i32]
@@ -186,6 +190,41 @@ def spark_attn_decode(qkv: torch.Tensor, gate: torch.Tensor, pos: torch.Tensor,
                                workspace.numel(), _stream(stream))
     if st != SPARK_OK:
         raise SparkError(st, "spark_attn_decode")
+    return out
+
+
+def spark_attn_decode_noalloc(qkv: torch.Tensor, gate: torch.Tensor, pos: torch.Tensor,
+                              k_cache: torch.Tensor, v_cache: torch.Tensor, layer,
+                              out: torch.Tensor | None = None,
+                              device_status: torch.Tensor | None = None,
+                              stream=None) -> torch.Tensor:
+    """spark_attn_decode without a workspace, for callers that cannot allocate
+    one: the split-KV scratch is a fixed buffer inside the library (see the
+    C header).  device_status: optional CUDA int32/uint32 tensor of one element
+    that receives the device fault bits."""
+    _need(qkv, torch.bfloat16, "qkv")
+    _need(gate, torch.float32, "gate")
+    _need(pos, torch.int32, "pos")
+    _need(k_cache, torch.bfloat16, "k_cache")
+    _need(v_cache, torch.bfloat16, "v_cache")
+    B, W = qkv.shape
+    H = gate.shape[-1]
+    Hkv = (W // HEAD_DIM - H) // 2
+    if (gate.shape != (B, H) or pos.shape != (B,) or k_cache.shape != v_cache.shape
+            or k_cache.shape[:2] != (B, Hkv) or k_cache.shape[3] != HEAD_DIM):
+        raise ValueError("inconsistent decode shapes")
+    if device_status is not None and (not device_status.is_cuda or device_status.numel() != 1
+                                      or device_status.element_size() != 4):
+        raise ValueError("device_status must be a one-element 32-bit CUDA tensor")
+    d = as_desc(layer)
+    if out is None:
+        out = torch.empty((B, H * HEAD_DIM), dtype=torch.bfloat16, device=qkv.device)
+    _need(out, torch.bfloat16, "out")
+    st = lib.spark_attn_decode_noalloc(_ptr(qkv), _ptr(gate), _ptr(pos), _ptr(k_cache),
+                                       _ptr(v_cache), k_cache.shape[2], ctypes.byref(d), B, H,
+                                       Hkv, _ptr(out), _ptr(device_status), _stream(stream))
+    if st != SPARK_OK:
+        raise SparkError(st, "spark_attn_decode_noalloc")
     return out
 
 

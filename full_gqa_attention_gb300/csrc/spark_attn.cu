@@ -417,3 +417,104 @@ spark_status spark_attn_read_status(void *workspace, uint32_t *status_out, int c
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- no-alloc decode
+//
+// A decode entry point for callers that cannot hand the library a workspace:
+// code running under a memory manager that owns every byte of device memory
+// (a serving runtime that reserves its pool up front, a plugin host that
+// passes only inputs and outputs), or code on a path where cudaMalloc is off
+// limits because it synchronizes the device.  The split-KV partial states
+// that spark_attn_decode keeps in the caller's workspace live here in one
+// fixed buffer owned by the library instead.  Every device that loads the
+// library holds this buffer until the process exits.
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // SPARK_NOALLOC_SCRATCH_BYTES
+
+// In host code this name is only a stand-in for the device buffer: the
+// device address comes from cudaGetSymbolAddress (see noalloc_scratch).
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mutex;
+void *g_noalloc_ptr[64] = {};
+
+// Device address of the scratch buffer on the current device, looked up once
+// per device (with that device current).  Returns nullptr on failure.
+void *noalloc_scratch() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_noalloc_ptr[dev] = p;
+    }
+    return g_noalloc_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" spark_status spark_attn_decode_noalloc(const void *qkv, const float *gate,
+                                                  const int32_t *pos, void *k_cache,
+                                                  void *v_cache, int64_t cap,
+                                                  const spark_layer_desc *desc, int B, int H,
+                                                  int Hkv, void *out, uint32_t *device_status,
+                                                  void *stream) {
+    spark_status st = check_decode(B, H, Hkv, cap, desc);
+    if (st != SPARK_OK) return st;
+    if (B == 0) return SPARK_OK;
+    if (!qkv || !gate || !pos || !k_cache || !v_cache || !out) return SPARK_ERR_NULL;
+    if (!aligned(qkv, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(gate, 4) || !aligned(pos, 4) || (device_status && !aligned(device_status, 4)))
+        return SPARK_ERR_ALIGN;
+    const DecodePlan pl = plan_decode(B, H, Hkv, cap, desc, sm_count_or_default());
+    if (pl.bytes > kNoAllocScratchBytes) return SPARK_ERR_WORKSPACE;
+    st = check_device();
+    if (st != SPARK_OK) return st;
+    uint8_t *ws = static_cast<uint8_t *>(noalloc_scratch());
+    if (!ws) return SPARK_ERR_CUDA;
+
+    DecodeParams P;
+    std::memset(&P, 0, sizeof(P));
+    P.qkv = static_cast<const __nv_bfloat16 *>(qkv);
+    P.gate = gate;
+    P.pos = pos;
+    P.k_cache = static_cast<__nv_bfloat16 *>(k_cache);
+    P.v_cache = static_cast<__nv_bfloat16 *>(v_cache);
+    P.out = static_cast<__nv_bfloat16 *>(out);
+    // Device-side fault bits go to the caller's word when one is given, else
+    // to a word of the scratch buffer that nobody reads.
+    P.status = device_status ? reinterpret_cast<unsigned *>(device_status)
+                             : reinterpret_cast<unsigned *>(ws);
+    P.part_ml = reinterpret_cast<float *>(ws + pl.ml_offset);
+    P.part_o = reinterpret_cast<float *>(ws + pl.o_offset);
+    P.cap = cap;
+    P.B = B;
+    P.H = H;
+    P.Hkv = Hkv;
+    P.G = H / Hkv;
+    P.kind = desc->kind;
+    P.window = desc->kind == SPARK_LAYER_SLIDING ? desc->window : 0;
+    P.nsplit = pl.nsplit;
+    P.chunk = pl.chunk;
+    make_rope_table(desc, &P.rope);
+
+    CUtensorMap tm_k, tm_v;
+    const uint64_t dims[4] = {static_cast<uint64_t>(kHeadDim), static_cast<uint64_t>(cap),
+                              static_cast<uint64_t>(Hkv), static_cast<uint64_t>(B)};
+    const uint64_t strides[3] = {kHeadDim * 2ull, static_cast<uint64_t>(cap) * kHeadDim * 2ull,
+                                 static_cast<uint64_t>(Hkv) * cap * kHeadDim * 2ull};
+    const uint32_t box[4] = {64, 64, 1, 1};
+    if (!encode_bf16(&tm_k, k_cache, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_bf16(&tm_v, v_cache, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+        return SPARK_ERR_CUDA;
+    return from_cuda(launch_decode(tm_k, tm_v, P, static_cast<cudaStream_t>(stream)));
+}

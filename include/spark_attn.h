@@ -148,6 +148,42 @@ spark_status spark_attn_decode(const void *qkv, const float *gate, const int32_t
                                void *stream);
 
 /*
+ * Decode without a caller-provided workspace.
+ *
+ * The paper has no counterpart to this call; it exists for callers that
+ * cannot allocate device memory for a workspace: code that runs under a
+ * memory manager owning all device memory (a serving runtime with a pool
+ * reserved up front, a plugin host that hands over only inputs and outputs),
+ * or code on a path where cudaMalloc is not allowed because it synchronizes
+ * the device.  It computes exactly what spark_attn_decode computes, with the
+ * same arguments except the workspace.  This call allocates nothing.
+ *
+ *  - Scratch: the split-KV partial states live in one library-owned device
+ *    buffer of SPARK_NOALLOC_SCRATCH_BYTES (8 MiB), held by every device that
+ *    loads the library until the process exits.  A call that would need more
+ *    (spark_attn_decode_workspace_size(...) > SPARK_NOALLOC_SCRATCH_BYTES,
+ *    e.g. large batches over long caches) returns SPARK_ERR_WORKSPACE and
+ *    enqueues nothing.  The buffer needs no zeroing: each call writes the
+ *    partial states it later reads.
+ *  - Sharing: all calls on a device share the buffer and it keeps the last
+ *    call's contents.  Calls that overlap on the GPU (different streams, or
+ *    several host threads without ordering) race on it and give wrong
+ *    results; order them on one stream.
+ *  - Set-up: the first call on each device looks up the buffer's device
+ *    address (cudaGetSymbolAddress, with that device current).  Make that
+ *    first call before any stream capture.
+ *  - device_status: optional DEVICE pointer to a uint32 that receives the
+ *    SPARK_DEVERR_* bits (OR-ed in, never cleared by the library); NULL
+ *    means those faults are not reported.
+ */
+#define SPARK_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+spark_status spark_attn_decode_noalloc(const void *qkv, const float *gate, const int32_t *pos,
+                                       void *k_cache, void *v_cache, int64_t cap,
+                                       const spark_layer_desc *desc, int B, int H, int Hkv,
+                                       void *out, uint32_t *device_status, void *stream);
+
+/*
  * Copies the sticky device status word out of a workspace (synchronizes on
  * `stream`).  If `clear` is non-zero the word is reset to 0 afterwards.
  */
