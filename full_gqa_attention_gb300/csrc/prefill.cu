@@ -15,11 +15,14 @@
 //         warp 0       TMA producer (Q tile once, then K and V through a ring
 //                      of 16 KB slots)
 //         warp 1       TMEM owner and MMA issuer (one thread)
-//         warps 4..7   softmax: thread i owns query row i (TMEM lane i)
+//         warps 4..11  softmax, two warpgroups: query row i (TMEM lane i) is
+//                      shared by thread i of each; warpgroup w owns score
+//                      columns [64w, 64w+64) and output dims [128w, 128w+128)
 //       TMEM (512 columns): O [128 x 256 fp32] in columns 0..255, two score
 //       buffers S0/S1 [128 x 128 fp32] in 256..383 and 384..511.  The
-//       probabilities P (bf16) overwrite the first 64 columns of their score
-//       buffer and feed P*V as the TMEM A operand.  QK^T of tile j+1 runs on
+//       probabilities P (bf16 pairs) overwrite columns 0..31 (keys 0..63) and
+//       64..95 (keys 64..127) of their score buffer, each warpgroup inside the
+//       columns it read, and feed P*V as the TMEM A operand.  QK^T of tile j+1 runs on
 //       the tensor cores while the softmax of tile j runs on the CUDA cores.
 //       Q is rotated in shared memory by the softmax threads (each its own
 //       row) before the first product.  Key tiles wholly outside the causal
@@ -88,8 +91,9 @@ constexpr int kBN = 128;                  // keys per tile
 constexpr int kSlotBytes = 16384;         // ring slot: 128 keys x 64 dims (K) or 32 keys x 256 (V)
 constexpr int kSlots = 8;
 constexpr int kQBytes = 4 * kSlotBytes;   // 128 rows x 256 dims, as 4 chunks of 64 dims
-constexpr int kAttnThreads = 256;
+constexpr int kAttnThreads = 384;
 constexpr int kSoftmaxWarp0 = 4;
+constexpr int kSoftmaxThreads = 256;        // two warpgroups, 64 score columns each
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0, kColS = 256;
 
@@ -103,7 +107,8 @@ constexpr int kBarPReady = 4 + 2 * kSlots;      // 2
 constexpr int kBarODone = 6 + 2 * kSlots;
 constexpr int kBarMmaDrain = 7 + 2 * kSlots;
 constexpr int kBarOFinal = 8 + 2 * kSlots;      // every P*V done (one phase per CTA)
-constexpr int kNumBars = 9 + 2 * kSlots;
+constexpr int kBarMaxX = 9 + 2 * kSlots;        // 2: half-row maxima exchanged (per tile parity)
+constexpr int kNumBars = 11 + 2 * kSlots;
 
 constexpr int kAttnSmemBytes = 1024 + kQBytes + kSlots * kSlotBytes + 256;
 
@@ -137,6 +142,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(ring + kSlots * kSlotBytes);
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
+    __shared__ float red_max[2][2][kBM];   // [tile parity][warpgroup][row]: half-row maxima
+    __shared__ float red_l[2][kBM];        // [warpgroup][row]: half-row sums
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = P.G, tq = kBM / G;
@@ -153,7 +160,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i) {
             uint32_t count = 1;
-            if (i == kBarQReady || i == kBarPReady || i == kBarPReady + 1) count = 128;
+            if (i == kBarQReady || i == kBarPReady || i == kBarPReady + 1 || i == kBarMaxX ||
+                i == kBarMaxX + 1)
+                count = kSoftmaxThreads;
             mbar_init(&bars[i], count);
         }
         fence_mbar_init();
@@ -282,7 +291,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         const int ks = vs * 2 + kk;  // 16-key step within the tile
                         const uint64_t bd = smem_desc_sw128(ring_addr + slot * kSlotBytes + kk * 2048,
                                                             kSlotBytes / 4, 1024);
-                        mma_ts(tmem + kColO, pcol + ks * 8, bd, kIdescPV, (j > 0 || ks > 0));
+                        // P of keys 0..63 sits in packed columns 0..31, keys 64..127 in 64..95
+                        const uint32_t acol = pcol + (ks < 4 ? ks * 8 : 64 + (ks - 4) * 8);
+                        mma_ts(tmem + kColO, acol, bd, kIdescPV, (j > 0 || ks > 0));
                     }
                     tc_commit(&bars[kBarSlotEmpty + slot]);
                     ++sc;
@@ -324,8 +335,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tmem_dealloc(tmem, kTmemCols);
     } else if (warp >= kSoftmaxWarp0) {
         // ------------------------------------------------------ softmax
-        const int row = tid - kSoftmaxWarp0 * 32;  // TMEM lane, query row
-        const int wq = warp - kSoftmaxWarp0;       // lane quarter of this warp
+        const int wq = warp & 3;                        // TMEM lane quarter of this warp
+        const int wg = (warp - kSoftmaxWarp0) >> 2;     // warpgroup: score-column half
+        const int row = wq * 32 + lane;                 // TMEM lane, query row
+        const int sth = tid - kSoftmaxWarp0 * 32;       // 0..255 among softmax threads
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const int tok = t0 + row / G;
         const int head = g * G + row % G;
@@ -335,10 +348,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const float gate_logit = valid ? P.gate[trow * P.H + head] : 0.f;
         bool ok = mbar_wait(&bars[kBarQFull], 0, &abort_flag, P.status);
 
-        // rotate this row of Q in place (bf16 in, fp32 math, bf16 out)
+        // rotate this row of Q in place (bf16 in, fp32 math, bf16 out); the
+        // two warpgroups take alternate groups of 8 pairs
         const int r = P.rope.rot_dim, half = r / 2;
         if (ok) {
-            for (int k0 = 0; k0 < half; k0 += 8) {
+            for (int k0 = wg * 8; k0 < half; k0 += 16) {
                 uint4 *pa = reinterpret_cast<uint4 *>(qbuf + sw128_offset(row, k0 / 8));
                 uint4 *pb = reinterpret_cast<uint4 *>(qbuf + sw128_offset(row, (k0 + half) / 8));
                 const uint4 a = *pa, bb = *pb;
@@ -362,53 +376,67 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         fence_proxy_async_smem();
         mbar_arrive(&bars[kBarQReady]);
 
+        // Scores stay in raw units s = q.k; probabilities are
+        // exp2(s * kScaleLog2 - m * kScaleLog2) with m the row's reference max.
+        // The reference moves only when the row max grows past it by the
+        // raw equivalent of 2^8.
+        constexpr float kLazyRaw = 8.0f / kScaleLog2;
         const int t_last = t_end - 1;
-        float m_run = -INFINITY, l_run = 0.f;
+        const int col0 = wg * 64;                       // first score column of this thread
+        float m_run = -INFINITY, l_part = 0.f;
         for (int j = 0; ok && j < ntiles; ++j) {
             ok = mbar_wait(&bars[kBarSFull + (j & 1)], (j >> 1) & 1, &abort_flag, P.status);
             if (!ok) break;
             tc_fence_after();
             const uint32_t sbase = lane_base + kColS + (j & 1) * kBN;
-            uint32_t sv[128];
-            tmem_ld32(sbase + 0, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-            tmem_ld32(sbase + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-            tmem_ld32(sbase + 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[64]));
-            tmem_ld32(sbase + 96, *reinterpret_cast<uint32_t(*)[32]>(&sv[96]));
+            uint32_t sv[64];
+            tmem_ld32(sbase + col0, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+            tmem_ld32(sbase + col0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
             tmem_ld_wait();
-            float x[128];
+            float x[64];
 #pragma unroll
-            for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sv[c]) * kScaleLog2;
+            for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(sv[c]);
             const int key0 = kv_lo + j * kBN;
             const bool need_mask = (key0 + kBN - 1 > t0) ||
                                    (P.kind == kLayerSliding && t_last - key0 >= P.window);
             if (need_mask) {
 #pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    const int key = key0 + c;
+                for (int c = 0; c < 64; ++c) {
+                    const int key = key0 + col0 + c;
                     const bool vis = key <= tok && (P.kind == kLayerFull || tok - key < P.window);
                     x[c] = vis ? x[c] : -INFINITY;
                 }
             }
-            float mx = x[0];
+            // row max of this half (8 independent chains), then of the row
+            float m8[8];
 #pragma unroll
-            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
-            const float m_new = fmaxf(m_run, mx);
-            // Move the reference maximum only when it grew by more than 2^8;
-            // what is already summed is then rescaled.  tcgen05.ld/st are
-            // warp-collective, so the O rescale runs for the whole warp (alpha
-            // is 1 on rows that keep their reference).
-            const bool bump = m_new > m_run + 8.0f;
+            for (int i = 0; i < 8; ++i) m8[i] = x[i];
+#pragma unroll
+            for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], x[c]);
+            const float mloc = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                     fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            // exchange with the other half of the row (a bounded wait, so a
+            // warp that gave up elsewhere cannot strand the others)
+            red_max[j & 1][wg][row] = mloc;
+            mbar_arrive(&bars[kBarMaxX + (j & 1)]);
+            ok = mbar_wait(&bars[kBarMaxX + (j & 1)], (j >> 1) & 1, &abort_flag, P.status);
+            if (!ok) break;
+            const float m_new = fmaxf(mloc, red_max[j & 1][wg ^ 1][row]);
+
+            // tcgen05.ld/st are warp-collective: the O rescale runs for the
+            // whole warp (alpha is 1 on rows that keep their reference)
+            const bool bump = m_new > m_run + kLazyRaw;
             const bool rescale_row = bump && m_run != -INFINITY;
-            const float alpha = rescale_row ? fast_exp2(m_run - m_new) : 1.f;
+            const float alpha = rescale_row ? fast_exp2((m_run - m_new) * kScaleLog2) : 1.f;
             if (bump) {
-                l_run *= alpha;
+                l_part *= alpha;
                 m_run = m_new;
             }
             if (j > 0 && __any_sync(0xffffffffu, rescale_row)) {
                 ok = mbar_wait(&bars[kBarODone], (j - 1) & 1, &abort_flag, P.status);
                 if (!ok) break;
                 tc_fence_after();
-                for (int c = 0; c < kHeadDim; c += 32) {
+                for (int c = wg * 128; c < wg * 128 + 128; c += 32) {
                     uint32_t ov[32];
                     tmem_ld32(lane_base + kColO + c, ov);
                     tmem_ld_wait();
@@ -418,19 +446,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     tmem_st32(lane_base + kColO + c, ov);
                 }
             }
-            const float z = (m_run == -INFINITY) ? 0.f : m_run;
-            uint32_t pk[64];
-            float lsum = 0.f;
+            const float neg = (m_run == -INFINITY) ? 0.f : -m_run * kScaleLog2;
+            uint32_t pk[32];
+            float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                const float p0 = fast_exp2(x[2 * c] - z);
-                const float p1 = fast_exp2(x[2 * c + 1] - z);
-                lsum += p0 + p1;
+            for (int c = 0; c < 32; ++c) {
+                const float p0 = fast_exp2(fmaf(x[2 * c], kScaleLog2, neg));
+                const float p1 = fast_exp2(fmaf(x[2 * c + 1], kScaleLog2, neg));
+                l8[c & 7] += p0 + p1;
                 pk[c] = pack_bf16x2(p0, p1);
             }
-            l_run += lsum;
-            tmem_st32(sbase + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-            tmem_st32(sbase + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+            l_part += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+            tmem_st32(sbase + wg * 64, pk);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bars[kBarPReady + (j & 1)]);
@@ -438,12 +465,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
         // epilogue: O / l * sigmoid(gate) -> bf16 -> staged in the Q buffer -> TMA store
         if (ok) ok = mbar_wait(&bars[kBarOFinal], 0, &abort_flag, P.status);
-        named_bar(1, 128);
-        const bool all_ok = !abort_flag;
-        if (all_ok) {
+        red_l[wg][row] = l_part;
+        named_bar(1, kSoftmaxThreads);
+        {
+            // every softmax thread runs this block (barrier counts must match);
+            // only the store below depends on the abort flag
             tc_fence_after();
-            const float scale = valid ? sigmoid_f32(gate_logit) / l_run : 0.f;
-            for (int c = 0; c < kHeadDim; c += 32) {
+            const float l_row = l_part + red_l[wg ^ 1][row];
+            const float scale = valid ? sigmoid_f32(gate_logit) / l_row : 0.f;
+            for (int c = wg * 128; c < wg * 128 + 128; c += 32) {
                 uint32_t ov[32];
                 tmem_ld32(lane_base + kColO + c, ov);
                 tmem_ld_wait();
@@ -462,8 +492,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
             }
             fence_proxy_async_smem();
-            named_bar(1, 128);
-            if (row == 0) {
+            named_bar(1, kSoftmaxThreads);
+            if (sth == 0 && !abort_flag) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
                     tma_store_4d(&tm_out, qbuf + c * kSlotBytes, c * 64, g * G, t0, b);
