@@ -372,17 +372,21 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant
     for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
     const float x_new = dot * kScaleLog2;
 
-    // merge the new token with the partial states of the non-empty splits
+    // merge the new token with the partial states of the non-empty splits:
+    // the maximum lane-parallel, then the weighted sums, several splits in flight
     const long long n_scan = (P.kind == kLayerFull) ? p : (p < P.cap ? p : P.cap);
     const int nvalid = static_cast<int>((n_scan + P.chunk - 1) / P.chunk);
     const size_t part0 = (static_cast<size_t>(b) * P.H + h) * P.nsplit;
     float M = x_new;
-    for (int sp = 0; sp < nvalid; ++sp) M = fmaxf(M, P.part_ml[2 * (part0 + sp)]);
+    for (int sp = lane; sp < nvalid; sp += 32) M = fmaxf(M, P.part_ml[2 * (part0 + sp)]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     const float w_new = fast_exp2(x_new - M);
     float L = w_new;
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = v[i] * w_new;
+#pragma unroll 4
     for (int sp = 0; sp < nvalid; ++sp) {
         const float2 ml = *reinterpret_cast<const float2 *>(P.part_ml + 2 * (part0 + sp));
         const float w = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M);

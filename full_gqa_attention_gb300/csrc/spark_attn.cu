@@ -163,8 +163,10 @@ struct DecodePlan {
 };
 
 // Splits the scanned slots of each (sequence, KV head) into equal chunks of a
-// multiple of 64 slots.  Small batches are spread over whole waves of the
-// GPU (one CTA per SM); large ones use chunks of at most 4096 slots.
+// multiple of 64 slots.  When there are fewer (sequence, KV head) pairs than
+// SMs, the chunks fill exactly one wave of the GPU (one CTA per SM streams one
+// long chunk, so no CTA starts late and few partial states are left to
+// merge); otherwise chunks of at most 4096 slots keep ragged batches balanced.
 DecodePlan plan_decode(int B, int H, int Hkv, int64_t cap, const spark_layer_desc *d, int sms) {
     DecodePlan pl{};
     long long max_scan = (d->kind == SPARK_LAYER_FULL) ? cap - 1 : cap;
@@ -172,11 +174,7 @@ DecodePlan plan_decode(int B, int H, int Hkv, int64_t cap, const spark_layer_des
     const long long kMaxChunk = 4096;
     const long long units = static_cast<long long>(B) * Hkv;
     long long ns = (max_scan + kMaxChunk - 1) / kMaxChunk;
-    if (units > 0 && units * ns <= 8LL * sms) {
-        const long long waves = (units * ns + sms - 1) / sms;
-        const long long fill = waves * sms / units;
-        if (fill > ns) ns = fill;
-    }
+    if (units > 0 && units <= sms) ns = sms / units;
     const long long max_ns = (max_scan + 63) / 64;
     if (ns > max_ns) ns = max_ns;
     if (ns < 1) ns = 1;
