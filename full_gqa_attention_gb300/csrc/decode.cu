@@ -64,6 +64,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+    grid_dep_wait();  // inputs and cache may come from the previous kernel
     const long long p = P.pos[b];
     if (p < 0 || (P.kind == kLayerFull && p >= P.cap)) {
         if (split == 0 && g == 0 && tid == 0) atomicOr(P.status, kErrPosition);
@@ -239,6 +240,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         if (lane == 0) mbar_arrive(&empty[s]);
     }
 
+    grid_dep_launch();  // the merge kernel may start its set-up
     // row sums over the 8 lanes that share this thread's heads
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
@@ -301,6 +303,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 __global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant__ DecodeParams P) {
     const int g = blockIdx.x, b = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    grid_dep_wait();  // partial states of the split kernel
+    grid_dep_launch();
     if (warp >= P.G) return;
     const int h = g * P.G + warp;
     const long long p = P.pos[b];
@@ -429,11 +433,11 @@ cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, cons
                                            kDecSmemBytes);
     if (err != cudaSuccess) return err;
     dim3 grid(P.nsplit, P.Hkv, P.B);
-    decode_split_kernel<<<grid, kDecThreads, kDecSmemBytes, stream>>>(tm_k, tm_v, P);
-    err = cudaGetLastError();
+    err = launch_overlapped(decode_split_kernel, grid, dim3(kDecThreads), kDecSmemBytes, stream,
+                            tm_k, tm_v, P);
     if (err != cudaSuccess) return err;
-    decode_merge_kernel<<<dim3(P.Hkv, P.B), 32 * P.G, 0, stream>>>(P);
-    return cudaGetLastError();
+    return launch_overlapped(decode_merge_kernel, dim3(P.Hkv, P.B), dim3(32 * P.G), 0, stream,
+                             P);
 }
 
 }  // namespace spark

@@ -43,6 +43,8 @@ __global__ void __launch_bounds__(kRopeThreads) prefill_rope_k_kernel(
     const int n_rot = half / 8;              // groups of 8 rotated pairs
     const int n_copy = (P.rot_w - r) / 8;    // groups of 8 dims copied unrotated
     const int items = n_rot + n_copy;
+    grid_dep_wait();  // qkv and pos may come from the previous kernel
+    grid_dep_launch();
     const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     const long long row = idx / items;
     const int it = static_cast<int>(idx % items);
@@ -183,6 +185,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
+    grid_dep_wait();  // rotated K (previous kernel) and every input are ready
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -464,6 +467,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
 
         // epilogue: O / l * sigmoid(gate) -> bf16 -> staged in the Q buffer -> TMA store
+        if (sth == 0) grid_dep_launch();
         if (ok) ok = mbar_wait(&bars[kBarOFinal], 0, &abort_flag, P.status);
         red_l[wg][row] = l_part;
         named_bar(1, kSoftmaxThreads);
@@ -520,8 +524,9 @@ cudaError_t launch_prefill(const CUtensorMap &tm_q, const CUtensorMap &tm_kv_k,
         const long long items = r / 16 + (P.rot_w - r) / 8;
         const long long threads = static_cast<long long>(P.B) * P.T * items;
         const long long blocks = (threads + kRopeThreads - 1) / kRopeThreads;
-        prefill_rope_k_kernel<<<static_cast<unsigned>(blocks), kRopeThreads, 0, stream>>>(P);
-        cudaError_t err = cudaGetLastError();
+        cudaError_t err = launch_overlapped(prefill_rope_k_kernel,
+                                            dim3(static_cast<unsigned>(blocks)),
+                                            dim3(kRopeThreads), 0, stream, P);
         if (err != cudaSuccess) return err;
     }
     cudaError_t err = cudaFuncSetAttribute(prefill_attn_kernel,
@@ -529,9 +534,8 @@ cudaError_t launch_prefill(const CUtensorMap &tm_q, const CUtensorMap &tm_kv_k,
                                            kAttnSmemBytes);
     if (err != cudaSuccess) return err;
     const unsigned grid = static_cast<unsigned>(P.n_qtiles) * P.Hkv * P.B;
-    prefill_attn_kernel<<<grid, kAttnThreads, kAttnSmemBytes, stream>>>(tm_q, tm_kv_k, tm_kv_v,
-                                                                        tm_krot, tm_out, P);
-    return cudaGetLastError();
+    return launch_overlapped(prefill_attn_kernel, dim3(grid), dim3(kAttnThreads), kAttnSmemBytes,
+                             stream, tm_q, tm_kv_k, tm_kv_v, tm_krot, tm_out, P);
 }
 
 }  // namespace spark

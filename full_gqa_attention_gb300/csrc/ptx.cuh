@@ -93,6 +93,21 @@ __device__ __forceinline__ bool mbar_wait_plain(uint64_t *bar, uint32_t parity) 
     }
 }
 
+// ---------------------------------------------------------------- launch overlap
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel on the stream drains.
+// It must wait (grid_dep_wait) before touching global memory that earlier
+// work writes; grid_dep_launch lets the next kernel start its own set-up.
+// Both are no-ops for a normal launch.
+
+__device__ __forceinline__ void grid_dep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
