@@ -125,6 +125,44 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int gran) {
                                  (((gran & 7) ^ (row & 7)) << 4));
 }
 
+// RoPE of one query row held in shared memory (the 128-byte-swizzled Q tile),
+// for the pair groups of warpgroup `wg`.  The G lanes holding the G heads of
+// one token compute 8/G of the 8 angles of a group each and exchange them by
+// shuffles, so each angle is computed once per token.
+template <int G>
+__device__ __forceinline__ void rotate_q_row(uint8_t *qbuf, int row, int lane, int wg, int pos,
+                                             const RopeTable &rope) {
+    const int half = rope.rot_dim / 2;
+    const int base = lane & ~(G - 1), sub = lane & (G - 1);
+    for (int k0 = wg * 8; k0 < half; k0 += 16) {
+        float cw[8 / G], sw[8 / G];
+#pragma unroll
+        for (int m = 0; m < 8 / G; ++m) rope_cos_sin(pos, rope.u[k0 + sub + G * m], cw[m], sw[m]);
+        float c[8], s[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            c[i] = __shfl_sync(0xffffffffu, cw[i / G], base + (i % G));
+            s[i] = __shfl_sync(0xffffffffu, sw[i / G], base + (i % G));
+        }
+        uint4 *pa = reinterpret_cast<uint4 *>(qbuf + sw128_offset(row, k0 / 8));
+        uint4 *pb = reinterpret_cast<uint4 *>(qbuf + sw128_offset(row, (k0 + half) / 8));
+        const uint4 a = *pa, bb = *pb;
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+        const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
+        uint32_t ya[4], yb[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float y1l, y2l, y1h, y2h;
+            rope_rotate(bf16_lo(aw[i]), bf16_lo(bw[i]), c[2 * i], s[2 * i], y1l, y2l);
+            rope_rotate(bf16_hi(aw[i]), bf16_hi(bw[i]), c[2 * i + 1], s[2 * i + 1], y1h, y2h);
+            ya[i] = pack_bf16x2(y1l, y1h);
+            yb[i] = pack_bf16x2(y2l, y2h);
+        }
+        *pa = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+        *pb = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+    }
+}
+
 __device__ __forceinline__ void named_bar(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -352,28 +390,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         bool ok = mbar_wait(&bars[kBarQFull], 0, &abort_flag, P.status);
 
         // rotate this row of Q in place (bf16 in, fp32 math, bf16 out); the
-        // two warpgroups take alternate groups of 8 pairs
-        const int r = P.rope.rot_dim, half = r / 2;
+        // two warpgroups take alternate groups of 8 pairs, and the G rows of a
+        // token (adjacent lanes) share the angles
         if (ok) {
-            for (int k0 = wg * 8; k0 < half; k0 += 16) {
-                uint4 *pa = reinterpret_cast<uint4 *>(qbuf + sw128_offset(row, k0 / 8));
-                uint4 *pb = reinterpret_cast<uint4 *>(qbuf + sw128_offset(row, (k0 + half) / 8));
-                const uint4 a = *pa, bb = *pb;
-                const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
-                const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
-                uint32_t ya[4], yb[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    float c0, s0, c1, s1, y1l, y2l, y1h, y2h;
-                    rope_cos_sin(p, P.rope.u[k0 + 2 * i], c0, s0);
-                    rope_cos_sin(p, P.rope.u[k0 + 2 * i + 1], c1, s1);
-                    rope_rotate(bf16_lo(aw[i]), bf16_lo(bw[i]), c0, s0, y1l, y2l);
-                    rope_rotate(bf16_hi(aw[i]), bf16_hi(bw[i]), c1, s1, y1h, y2h);
-                    ya[i] = pack_bf16x2(y1l, y1h);
-                    yb[i] = pack_bf16x2(y2l, y2h);
-                }
-                *pa = make_uint4(ya[0], ya[1], ya[2], ya[3]);
-                *pb = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+            switch (G) {
+                case 1: rotate_q_row<1>(qbuf, row, lane, wg, p, P.rope); break;
+                case 2: rotate_q_row<2>(qbuf, row, lane, wg, p, P.rope); break;
+                case 4: rotate_q_row<4>(qbuf, row, lane, wg, p, P.rope); break;
+                default: rotate_q_row<8>(qbuf, row, lane, wg, p, P.rope); break;
             }
         }
         fence_proxy_async_smem();
