@@ -76,10 +76,10 @@ class OracleLib:
         i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
         lib.oracle_rope.argtypes = [P, P, i64, i32, f64, P]
         lib.oracle_rope.restype = i32
-        lib.oracle_prefill.argtypes = [P, P, P, i32, i32, f64, i32, i32, i32,
+        lib.oracle_prefill.argtypes = [P, P, P, i32, i32, f64, i32, i32, i32, i32,
                                        i32, i32, P, i64, P]
         lib.oracle_prefill.restype = i32
-        lib.oracle_decode.argtypes = [P, P, P, P, P, i64, i32, i32, f64, i32,
+        lib.oracle_decode.argtypes = [P, P, P, P, P, i64, i32, i32, f64, i32, i32,
                                       i32, i32, i32, P, P, P]
         lib.oracle_decode.restype = i32
         self.path = path
@@ -98,7 +98,7 @@ class OracleLib:
 
     def prefill(self, qkv_bits: np.ndarray, gate: np.ndarray, pos: np.ndarray,
                 kind: int, window: int, theta: float, rot_dim: int, H: int, Hkv: int,
-                rows: np.ndarray | None = None) -> np.ndarray:
+                rows: np.ndarray | None = None, gate_mode: int = 0) -> np.ndarray:
         """Oracle prefill.
 
         qkv_bits: uint16 [B, T, (H+2Hkv)*256] (bf16 patterns); gate: fp32
@@ -118,13 +118,14 @@ class OracleLib:
             out = np.empty((B, T, H * HEAD_DIM), np.float64)
             n = B * T
         _check(self._lib.oracle_prefill(_ptr(qkv_bits), _ptr(gate), _ptr(pos), kind,
-                                        window, float(theta), rot_dim, B, T, H, Hkv,
-                                        _ptr(rows), n, _ptr(out)), "prefill")
+                                        window, float(theta), rot_dim, gate_mode, B, T, H,
+                                        Hkv, _ptr(rows), n, _ptr(out)), "prefill")
         return out
 
     def decode(self, qkv_bits: np.ndarray, gate: np.ndarray, pos: np.ndarray,
                k_cache_bits: np.ndarray, v_cache_bits: np.ndarray, kind: int,
-               window: int, theta: float, rot_dim: int, H: int, Hkv: int):
+               window: int, theta: float, rot_dim: int, H: int, Hkv: int,
+               gate_mode: int = 0):
         """Oracle decode step (write-then-attend).
 
         qkv_bits: uint16 [B, (H+2Hkv)*256]; gate: fp32 [B, H]; pos: int32 [B];
@@ -149,8 +150,8 @@ class OracleLib:
         v_new = np.empty((B, Hkv, HEAD_DIM), np.float64)
         _check(self._lib.oracle_decode(_ptr(qkv_bits), _ptr(gate), _ptr(pos),
                                        _ptr(k_cache_bits), _ptr(v_cache_bits), cap,
-                                       kind, window, float(theta), rot_dim, B, H, Hkv,
-                                       _ptr(out), _ptr(k_new), _ptr(v_new)), "decode")
+                                       kind, window, float(theta), rot_dim, gate_mode, B, H,
+                                       Hkv, _ptr(out), _ptr(k_new), _ptr(v_new)), "decode")
         return out, k_new, v_new
 
 

@@ -20,6 +20,8 @@
  *    first rotary_dim channels of every head and leaves the rest unchanged.
  *  - Same page, §2 "hybrid attention": full layers use a causal mask, sliding
  *    layers a sliding-window causal mask of window 512.
+ *    The gate activation is sigmoid; the page notes the code also supports
+ *    silu (gate_attn_act_mode), which multiplies by x * sigmoid(x) instead.
  *  - Spark-X2.5-4B hybrid-attention explainer (lshu.cn), section on the
  *    sliding layer's KV cache: a sliding layer keeps only the latest 512
  *    tokens; older ones are dropped.  Full layers keep every token.
@@ -62,6 +64,17 @@ static double bf16_bits_to_f64(uint16_t bits)
 }
 
 static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+/*
+ * Gate activation (Spark-X2.5 architecture, §3): the released checkpoints use
+ * sigmoid; the code also supports silu, x * sigmoid(x).
+ */
+enum { ORACLE_GATE_SIGMOID = 0, ORACLE_GATE_SILU = 1 };
+
+static double gate_act(double x, int mode)
+{
+    return mode == ORACLE_GATE_SILU ? x * sigmoid(x) : sigmoid(x);
+}
 
 /*
  * RoPE on one head vector x[0..255] at position pos, written to y.
@@ -107,7 +120,7 @@ int oracle_rope(const double *x, const int32_t *pos, int64_t n, int rot_dim,
  */
 static void attend_one(const double *q, const double *const *keys,
                        const double *const *vals, int64_t nvis, double gate_logit,
-                       double *s_scratch, double *out)
+                       int gate_mode, double *s_scratch, double *out)
 {
     const double scale = 1.0 / sqrt((double)ORACLE_HEAD_DIM);
     double m = -INFINITY;
@@ -131,7 +144,7 @@ static void attend_one(const double *q, const double *const *keys,
         for (int d = 0; d < ORACLE_HEAD_DIM; ++d)
             out[d] += p * vals[j][d];
     }
-    double gsig = sigmoid(gate_logit);
+    double gsig = gate_act(gate_logit, gate_mode);
     for (int d = 0; d < ORACLE_HEAD_DIM; ++d)
         out[d] *= gsig;
 }
@@ -153,13 +166,14 @@ static int64_t first_visible(int kind, int window, int64_t i)
  * The mask is on the token index inside the sequence; RoPE uses pos.
  */
 int oracle_prefill(const uint16_t *qkv, const float *gate, const int32_t *pos,
-                   int kind, int window, double theta, int rot_dim, int B, int T,
-                   int H, int Hkv, const int64_t *rows, int64_t nrows, double *out)
+                   int kind, int window, double theta, int rot_dim, int gate_mode, int B,
+                   int T, int H, int Hkv, const int64_t *rows, int64_t nrows, double *out)
 {
     if (!qkv || !gate || !pos || !out || B <= 0 || T <= 0 || H <= 0 || Hkv <= 0 ||
         H % Hkv != 0 || rot_dim < 0 || rot_dim > ORACLE_HEAD_DIM || (rot_dim & 1) ||
         (kind != ORACLE_FULL && kind != ORACLE_SLIDING) ||
-        (kind == ORACLE_SLIDING && window < 1))
+        (kind == ORACLE_SLIDING && window < 1) ||
+        (gate_mode != ORACLE_GATE_SIGMOID && gate_mode != ORACLE_GATE_SILU))
         return ORACLE_ERR_ARG;
     if (!rows)
         nrows = (int64_t)B * T;
@@ -218,7 +232,7 @@ int oracle_prefill(const uint16_t *qkv, const float *gate, const int32_t *pos,
                         kp[j] = krot + (tok * Hkv + g) * D;
                         vp[j] = vf + (tok * Hkv + g) * D;
                     }
-                    attend_one(q, kp, vp, nvis, (double)gate[row * H + h], s,
+                    attend_one(q, kp, vp, nvis, (double)gate[row * H + h], gate_mode, s,
                                out + ri * (int64_t)H * D + (int64_t)h * D);
                 }
             }
@@ -248,13 +262,14 @@ int oracle_prefill(const uint16_t *qkv, const float *gate, const int32_t *pos,
  */
 int oracle_decode(const uint16_t *qkv, const float *gate, const int32_t *pos,
                   const uint16_t *k_cache, const uint16_t *v_cache, int64_t cap,
-                  int kind, int window, double theta, int rot_dim, int B, int H,
-                  int Hkv, double *out, double *k_new, double *v_new)
+                  int kind, int window, double theta, int rot_dim, int gate_mode, int B,
+                  int H, int Hkv, double *out, double *k_new, double *v_new)
 {
     if (!qkv || !gate || !pos || !k_cache || !v_cache || !out || B <= 0 || H <= 0 ||
         Hkv <= 0 || H % Hkv != 0 || rot_dim < 0 || rot_dim > ORACLE_HEAD_DIM ||
         (rot_dim & 1) || cap <= 0 || (kind != ORACLE_FULL && kind != ORACLE_SLIDING) ||
-        (kind == ORACLE_SLIDING && (window < 1 || cap < window)))
+        (kind == ORACLE_SLIDING && (window < 1 || cap < window)) ||
+        (gate_mode != ORACLE_GATE_SIGMOID && gate_mode != ORACLE_GATE_SILU))
         return ORACLE_ERR_ARG;
     for (int b = 0; b < B; ++b)
         if (pos[b] < 0 || (kind == ORACLE_FULL && (int64_t)pos[b] + 1 > cap))
@@ -350,7 +365,7 @@ int oracle_decode(const uint16_t *qkv, const float *gate, const int32_t *pos,
                         o[d] += pj * bf16_bits_to_f64(vc[slot * D + d]);
                 }
             }
-            double gsig = sigmoid((double)gate[(int64_t)b * H + h]);
+            double gsig = gate_act((double)gate[(int64_t)b * H + h], gate_mode);
             double *dst = out + (int64_t)b * H * D + (int64_t)h * D;
             for (int d = 0; d < D; ++d)
                 dst[d] = o[d] * gsig;

@@ -40,8 +40,13 @@ def visible(kind: int, window: int, T: int) -> np.ndarray:
     return m
 
 
+def gate_activation(g, gate_mode: int):
+    """sigmoid (mode 0) or silu = g * sigmoid(g) (mode 1), from scipy's expit."""
+    return expit(g) if gate_mode == 0 else g * expit(g)
+
+
 def prefill(qkv: np.ndarray, gate: np.ndarray, pos: np.ndarray, kind: int,
-            window: int, theta: float, rot_dim: int, H: int, Hkv: int):
+            window: int, theta: float, rot_dim: int, H: int, Hkv: int, gate_mode: int = 0):
     """qkv fp64 [B,T,(H+2Hkv)*256], gate [B,T,H], pos [B,T] -> fp64 [B,T,H*256]."""
     B, T, _ = qkv.shape
     G = H // Hkv
@@ -58,13 +63,13 @@ def prefill(qkv: np.ndarray, gate: np.ndarray, pos: np.ndarray, kind: int,
             s = q[b, :, h, :] @ k[b, :, g, :].T / np.sqrt(D)
             s = np.where(mask, s, -np.inf)
             p = softmax(s, axis=-1)
-            out[b, :, h, :] = (p @ v[b, :, g, :]) * expit(gate[b, :, h])[:, None]
+            out[b, :, h, :] = (p @ v[b, :, g, :]) * gate_activation(gate[b, :, h], gate_mode)[:, None]
     return out.reshape(B, T, H * D)
 
 
 def decode(qkv: np.ndarray, gate: np.ndarray, pos: np.ndarray, k_cache: np.ndarray,
            v_cache: np.ndarray, kind: int, window: int, theta: float, rot_dim: int,
-           H: int, Hkv: int):
+           H: int, Hkv: int, gate_mode: int = 0):
     """One decode step by brute force.
 
     qkv fp64 [B,(H+2Hkv)*256]; gate [B,H]; pos [B]; caches fp64 [B,Hkv,cap,256]
@@ -91,5 +96,5 @@ def decode(qkv: np.ndarray, gate: np.ndarray, pos: np.ndarray, k_cache: np.ndarr
             vals = np.stack([vn[g] if t == p else v_cache[b, g, t % cap if kind == 1 else t]
                              for t in toks])
             w = softmax(keys @ q[h] / np.sqrt(D))
-            out[b, h] = (w @ vals) * expit(gate[b, h])
+            out[b, h] = (w @ vals) * gate_activation(gate[b, h], gate_mode)
     return out.reshape(B, H * D)

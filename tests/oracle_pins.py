@@ -351,6 +351,31 @@ def pin_decode_new_entries(orc):
     assert np.array_equal(vn, v)
 
 
+def pin_silu_gate(orc):
+    """The silu gate (gate_attn_act_mode, §3): brute force agrees, a zero logit
+    gives exactly zero, and a logit of 40 (sigmoid == 1 in fp64) gives 40x the
+    ungated output."""
+    H, Hkv, B, T = 4, 2, 2, 7
+    bits, x = bf16_inputs(111, (B, T, (H + 2 * Hkv) * D))
+    g = gates(112, (B, T, H), std=2.0)
+    pos = _positions("random", B, T, 113)
+    got = orc.prefill(bits, g, pos, SLIDING, 3, 1e4, 256, H, Hkv, gate_mode=1)
+    want = brute.prefill(x, g.astype(np.float64), pos, SLIDING, 3, 1e4, 256, H, Hkv, gate_mode=1)
+    assert np.max(np.abs(got - want)) < 1e-9
+    zero = orc.prefill(bits, np.zeros_like(g), pos, FULL, 0, 5e6, 64, H, Hkv, gate_mode=1)
+    assert not np.any(zero)
+    big = orc.prefill(bits, np.full_like(g, 40.0), pos, FULL, 0, 5e6, 64, H, Hkv, gate_mode=1)
+    ungated = orc.prefill(bits, np.full_like(g, 40.0), pos, FULL, 0, 5e6, 64, H, Hkv)
+    assert np.allclose(big, 40.0 * ungated, rtol=1e-15, atol=0)
+    kb, kx = bf16_inputs(114, (B, Hkv, 9, D))
+    dpos = np.array([8, 3], np.int32)
+    dg = gates(115, (B, H), std=2.0)
+    got, _, _ = orc.decode(bits[:, 0], dg, dpos, kb, kb, FULL, 0, 5e6, 64, H, Hkv, gate_mode=1)
+    want = brute.decode(x[:, 0], dg.astype(np.float64), dpos, kx, kx, FULL, 0, 5e6, 64, H, Hkv,
+                        gate_mode=1)
+    assert np.max(np.abs(got - want)) < 1e-9
+
+
 ALL_PINS = [
     pin_brute_force,
     pin_decode_brute_force,
@@ -368,4 +393,5 @@ ALL_PINS = [
     pin_decode_equals_prefill_last_row,
     pin_decode_ring_wrap,
     pin_decode_new_entries,
+    pin_silu_gate,
 ]

@@ -40,6 +40,8 @@ MUTANTS = [
     ("gate_dropped_prefill", "out[d] *= gsig;", "out[d] *= 1.0;"),
     ("gate_dropped_decode", "dst[d] = o[d] * gsig;", "dst[d] = o[d];"),
     ("sigmoid_sign", "1.0 / (1.0 + exp(-x))", "1.0 / (1.0 + exp(x))"),
+    ("silu_without_x", "mode == ORACLE_GATE_SILU ? x * sigmoid(x) : sigmoid(x)",
+     "mode == ORACLE_GATE_SILU ? sigmoid(x) : sigmoid(x)"),
     ("group_map_modulo", "int g = h / G;", "int g = h % Hkv;"),
     ("v_from_k_slot", "(int64_t)(H + Hkv + g) * D", "(int64_t)(H + g) * D"),
     ("softmax_sign", "exp(s_scratch[j] - m)", "exp(m - s_scratch[j])"),
