@@ -8,6 +8,7 @@ from ._binding import (  # noqa: F401
     SPARK_DEVERR_POSITION,
     SPARK_DEVERR_TIMEOUT,
     SPARK_GATE_SIGMOID,
+    SPARK_GATE_SILU,
     SPARK_LAYER_FULL,
     SPARK_LAYER_SLIDING,
     SPARK_NOALLOC_SCRATCH_BYTES,
@@ -21,6 +22,7 @@ from ._binding import (  # noqa: F401
     spark_attn_decode_noalloc,
     spark_attn_decode_workspace_size,
     spark_attn_prefill,
+    spark_attn_prefill_cache,
     spark_attn_prefill_workspace_size,
     spark_attn_read_status,
     spark_attn_version,

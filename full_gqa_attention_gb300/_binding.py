@@ -28,6 +28,7 @@ SPARK_ERR_DEVICE = 8
 SPARK_LAYER_FULL = 0
 SPARK_LAYER_SLIDING = 1
 SPARK_GATE_SIGMOID = 0
+SPARK_GATE_SILU = 1
 
 SPARK_NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -55,6 +56,9 @@ def _load() -> ctypes.CDLL:
     lib.spark_attn_prefill_workspace_size.restype = sz
     lib.spark_attn_prefill.argtypes = [P, P, P, D, i32, i32, i32, i32, P, P, sz, P]
     lib.spark_attn_prefill.restype = i32
+    lib.spark_attn_prefill_cache.argtypes = [P, P, P, P, P, i64, D, i32, i32, i32, i32, P, P,
+                                             sz, P]
+    lib.spark_attn_prefill_cache.restype = i32
     lib.spark_attn_decode_workspace_size.argtypes = [i32, i32, i32, i64, D]
     lib.spark_attn_decode_workspace_size.restype = sz
     lib.spark_attn_decode.argtypes = [P, P, P, P, P, i64, D, i32, i32, i32, P, P, sz, P]
@@ -157,6 +161,40 @@ def spark_attn_prefill(qkv: torch.Tensor, gate: torch.Tensor, pos: torch.Tensor,
                                 _stream(stream))
     if st != SPARK_OK:
         raise SparkError(st, "spark_attn_prefill")
+    return out
+
+
+def spark_attn_prefill_cache(qkv: torch.Tensor, gate: torch.Tensor, pos: torch.Tensor,
+                             k_cache: torch.Tensor, v_cache: torch.Tensor, layer,
+                             out: torch.Tensor | None = None,
+                             workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Prefill that also stores rotated K and V in the decode cache
+    (caches bf16 [B,Hkv,cap,256]; see spark_attn_prefill for the rest)."""
+    _need(qkv, torch.bfloat16, "qkv")
+    _need(gate, torch.float32, "gate")
+    _need(pos, torch.int32, "pos")
+    _need(k_cache, torch.bfloat16, "k_cache")
+    _need(v_cache, torch.bfloat16, "v_cache")
+    B, T, W = qkv.shape
+    H = gate.shape[-1]
+    Hkv = (W // HEAD_DIM - H) // 2
+    if (gate.shape != (B, T, H) or pos.shape != (B, T) or (H + 2 * Hkv) * HEAD_DIM != W
+            or k_cache.shape != v_cache.shape or k_cache.shape[:2] != (B, Hkv)
+            or k_cache.shape[3] != HEAD_DIM):
+        raise ValueError("inconsistent prefill shapes")
+    d = as_desc(layer)
+    if out is None:
+        out = torch.empty((B, T, H * HEAD_DIM), dtype=torch.bfloat16, device=qkv.device)
+    _need(out, torch.bfloat16, "out")
+    need = lib.spark_attn_prefill_workspace_size(B, T, H, Hkv, ctypes.byref(d))
+    if workspace is None:
+        workspace = new_workspace(need, qkv.device)
+    st = lib.spark_attn_prefill_cache(_ptr(qkv), _ptr(gate), _ptr(pos), _ptr(k_cache),
+                                      _ptr(v_cache), k_cache.shape[2], ctypes.byref(d), B, T, H,
+                                      Hkv, _ptr(out), _ptr(workspace), workspace.numel(),
+                                      _stream(stream))
+    if st != SPARK_OK:
+        raise SparkError(st, "spark_attn_prefill_cache")
     return out
 
 

@@ -61,6 +61,12 @@ __device__ __forceinline__ void rope_rotate(float x1, float x2, float c, float s
 
 __device__ __forceinline__ float sigmoid_f32(float x) { return 1.0f / (1.0f + expf(-x)); }
 
+// Gate activation of the output gate: sigmoid (mode 0) or silu (mode 1).
+__device__ __forceinline__ float gate_act(float x, int mode) {
+    const float s = sigmoid_f32(x);
+    return mode == 1 ? x * s : s;
+}
+
 // Launches `kernel` allowing programmatic dependent launch: it may be
 // scheduled before the previous kernel on the stream has finished, and waits
 // for it with grid_dep_wait before reading global memory.
@@ -95,6 +101,7 @@ struct DecodeParams {
     long long cap;             // cache slots per (b, kv head)
     int B, H, Hkv, G;
     int kind, window;
+    int gate_mode;             // 0 sigmoid, 1 silu
     int nsplit;                // splits per (b, kv head)
     int chunk;                 // scanned slots per split (multiple of 64)
     RopeTable rope;
@@ -107,9 +114,13 @@ struct PrefillParams {
     const float *gate;         // [B, T, H]
     const int32_t *pos;        // [B, T]
     __nv_bfloat16 *krot;       // [B, Hkv, T, rot_w]: rotated leading dims of K
+    __nv_bfloat16 *k_cache;    // optional [B, Hkv, cap, 256]: receives rotated K
+    __nv_bfloat16 *v_cache;    // optional [B, Hkv, cap, 256]: receives V
+    long long cap;             // cache slots (when k_cache is set)
     unsigned *status;
     int B, T, H, Hkv, G;
     int kind, window;
+    int gate_mode;             // 0 sigmoid, 1 silu
     int rot_w;                 // rot_dim rounded up to 64: leading K dims read from krot
     int n_qtiles;              // query tiles per (b, kv head)
     RopeTable rope;

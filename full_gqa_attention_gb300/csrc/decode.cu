@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant
         acc[6] += c.z * w;
         acc[7] += c.w * w;
     }
-    const float scale = sigmoid_f32(P.gate[static_cast<size_t>(b) * P.H + h]) / L;
+    const float scale = gate_act(P.gate[static_cast<size_t>(b) * P.H + h], P.gate_mode) / L;
     uint4 ov;
     ov.x = pack_bf16x2(acc[0] * scale, acc[1] * scale);
     ov.y = pack_bf16x2(acc[2] * scale, acc[3] * scale);

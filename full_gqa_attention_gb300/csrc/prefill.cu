@@ -86,6 +86,70 @@ __global__ void __launch_bounds__(kRopeThreads) prefill_rope_k_kernel(
     }
 }
 
+// ---------------------------------------------------------------- KV cache fill
+
+// Stores every token's rotated K (all 256 dims) and its V in the decode cache,
+// the step a model takes while it prefills (past_key_values.update): token t
+// goes to slot t of a full layer's cache, or to slot t mod cap of a sliding
+// layer's ring, where only the last cap tokens survive.  One thread per
+// (token, group of 8 rotated pairs / 8 copied K dims / 8 V dims), looping over
+// KV heads so each angle is computed once per (token, pair).
+__global__ void __launch_bounds__(kRopeThreads) prefill_store_kv_kernel(
+    const __grid_constant__ PrefillParams P) {
+    grid_dep_wait();
+    grid_dep_launch();
+    const int r = P.rope.rot_dim, half = r / 2;
+    const int n_rot = half / 8, n_kcopy = (kHeadDim - r) / 8, n_v = kHeadDim / 8;
+    const int items = n_rot + n_kcopy + n_v;
+    const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long row = idx / items;
+    const int it = static_cast<int>(idx % items);
+    if (row >= static_cast<long long>(P.B) * P.T) return;
+    const int b = static_cast<int>(row / P.T), t = static_cast<int>(row % P.T);
+    if (P.kind == kLayerSliding && t < P.T - P.cap) return;  // overwritten later in the ring
+    const long long slot = (P.kind == kLayerFull) ? t : t % P.cap;
+    const size_t width = static_cast<size_t>(P.H + 2 * P.Hkv) * kHeadDim;
+    const __nv_bfloat16 *src_k = P.qkv + row * width + static_cast<size_t>(P.H) * kHeadDim;
+    const __nv_bfloat16 *src_v = src_k + static_cast<size_t>(P.Hkv) * kHeadDim;
+    const size_t head_stride = static_cast<size_t>(P.cap) * kHeadDim;
+    const size_t base = (static_cast<size_t>(b) * P.Hkv * P.cap + slot) * kHeadDim;
+    if (it < n_rot) {
+        const int k0 = it * 8;
+        const int p = P.pos[row];
+        float c[8], s[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rope_cos_sin(p, P.rope.u[k0 + i], c[i], s[i]);
+        for (int g = 0; g < P.Hkv; ++g) {
+            const uint4 a = *reinterpret_cast<const uint4 *>(src_k + g * kHeadDim + k0);
+            const uint4 bb = *reinterpret_cast<const uint4 *>(src_k + g * kHeadDim + k0 + half);
+            const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+            const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
+            uint32_t ya[4], yb[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float y1l, y2l, y1h, y2h;
+                rope_rotate(bf16_lo(aw[i]), bf16_lo(bw[i]), c[2 * i], s[2 * i], y1l, y2l);
+                rope_rotate(bf16_hi(aw[i]), bf16_hi(bw[i]), c[2 * i + 1], s[2 * i + 1], y1h, y2h);
+                ya[i] = pack_bf16x2(y1l, y1h);
+                yb[i] = pack_bf16x2(y2l, y2h);
+            }
+            __nv_bfloat16 *dst = P.k_cache + base + g * head_stride;
+            *reinterpret_cast<uint4 *>(dst + k0) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+            *reinterpret_cast<uint4 *>(dst + k0 + half) = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+        }
+    } else if (it < n_rot + n_kcopy) {
+        const int d0 = r + (it - n_rot) * 8;
+        for (int g = 0; g < P.Hkv; ++g)
+            *reinterpret_cast<uint4 *>(P.k_cache + base + g * head_stride + d0) =
+                *reinterpret_cast<const uint4 *>(src_k + g * kHeadDim + d0);
+    } else {
+        const int d0 = (it - n_rot - n_kcopy) * 8;
+        for (int g = 0; g < P.Hkv; ++g)
+            *reinterpret_cast<uint4 *>(P.v_cache + base + g * head_stride + d0) =
+                *reinterpret_cast<const uint4 *>(src_v + g * kHeadDim + d0);
+    }
+}
+
 // ---------------------------------------------------------------- attention
 
 constexpr int kBM = 128;                  // query rows per tile
@@ -500,7 +564,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             // only the store below depends on the abort flag
             tc_fence_after();
             const float l_row = l_part + red_l[wg ^ 1][row];
-            const float scale = valid ? sigmoid_f32(gate_logit) / l_row : 0.f;
+            const float scale = valid ? gate_act(gate_logit, P.gate_mode) / l_row : 0.f;
             for (int c = wg * 128; c < wg * 128 + 128; c += 32) {
                 uint32_t ov[32];
                 tmem_ld32(lane_base + kColO + c, ov);
@@ -558,8 +622,16 @@ cudaError_t launch_prefill(const CUtensorMap &tm_q, const CUtensorMap &tm_kv_k,
                                            kAttnSmemBytes);
     if (err != cudaSuccess) return err;
     const unsigned grid = static_cast<unsigned>(P.n_qtiles) * P.Hkv * P.B;
-    return launch_overlapped(prefill_attn_kernel, dim3(grid), dim3(kAttnThreads), kAttnSmemBytes,
-                             stream, tm_q, tm_kv_k, tm_kv_v, tm_krot, tm_out, P);
+    err = launch_overlapped(prefill_attn_kernel, dim3(grid), dim3(kAttnThreads), kAttnSmemBytes,
+                            stream, tm_q, tm_kv_k, tm_kv_v, tm_krot, tm_out, P);
+    if (err != cudaSuccess || P.k_cache == nullptr) return err;
+    // fill the decode cache (it reads only qkv and pos)
+    const int r = P.rope.rot_dim;
+    const long long items = r / 16 + (kHeadDim - r) / 8 + kHeadDim / 8;
+    const long long threads = static_cast<long long>(P.B) * P.T * items;
+    const long long blocks = (threads + kRopeThreads - 1) / kRopeThreads;
+    return launch_overlapped(prefill_store_kv_kernel, dim3(static_cast<unsigned>(blocks)),
+                             dim3(kRopeThreads), 0, stream, P);
 }
 
 }  // namespace spark

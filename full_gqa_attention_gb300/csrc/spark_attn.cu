@@ -128,7 +128,8 @@ spark_status check_layer(const spark_layer_desc *d, int H, int Hkv) {
     if (!(d->rope_theta > 0.0) || !std::isfinite(d->rope_theta)) return SPARK_ERR_SHAPE;
     if (d->rot_dim < 0 || d->rot_dim > SPARK_HEAD_DIM || (d->rot_dim & 1)) return SPARK_ERR_SHAPE;
     if (d->rot_dim % 16 != 0) return SPARK_ERR_UNSUPPORTED;
-    if (d->gate_mode != SPARK_GATE_SIGMOID) return SPARK_ERR_UNSUPPORTED;
+    if (d->gate_mode != SPARK_GATE_SIGMOID && d->gate_mode != SPARK_GATE_SILU)
+        return SPARK_ERR_UNSUPPORTED;
     const int G = H / Hkv;
     if (G != 1 && G != 2 && G != 4 && G != 8) return SPARK_ERR_UNSUPPORTED;
     return SPARK_OK;
@@ -225,6 +226,96 @@ spark_status check_prefill(int B, int T, int H, int Hkv, const spark_layer_desc 
     return SPARK_OK;
 }
 
+// Prefill, optionally filling the decode cache (k_cache != nullptr).
+spark_status prefill_impl(const void *qkv, const float *gate, const int32_t *pos,
+                          const spark_layer_desc *desc, int B, int T, int H, int Hkv, void *out,
+                          void *k_cache, void *v_cache, int64_t cap, void *workspace,
+                          size_t workspace_bytes, void *stream) {
+    spark_status st = check_prefill(B, T, H, Hkv, desc);
+    if (st != SPARK_OK) return st;
+    if (k_cache || v_cache) {
+        if (cap < 1) return SPARK_ERR_CAPACITY;
+        if (desc->kind == SPARK_LAYER_FULL && cap < T) return SPARK_ERR_CAPACITY;
+        if (desc->kind == SPARK_LAYER_SLIDING && cap < desc->window) return SPARK_ERR_CAPACITY;
+        if (cap > 0x7fffffffLL) return SPARK_ERR_UNSUPPORTED;
+    }
+    if (B == 0 || T == 0) return SPARK_OK;
+    if (!qkv || !gate || !pos || !out || !workspace) return SPARK_ERR_NULL;
+    if ((k_cache == nullptr) != (v_cache == nullptr)) return SPARK_ERR_NULL;
+    if (!aligned(qkv, 16) || !aligned(out, 16) || !aligned(gate, 4) || !aligned(pos, 4) ||
+        !aligned(workspace, 256) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return SPARK_ERR_ALIGN;
+    const PrefillPlan pl = plan_prefill(B, T, Hkv, desc);
+    if (workspace_bytes < pl.bytes) return SPARK_ERR_WORKSPACE;
+    st = check_device();
+    if (st != SPARK_OK) return st;
+
+    const int G = H / Hkv;
+    const int tq = kPrefillRows / G;  // tokens per query tile
+    PrefillParams P;
+    std::memset(&P, 0, sizeof(P));
+    P.qkv = static_cast<const __nv_bfloat16 *>(qkv);
+    P.gate = gate;
+    P.pos = pos;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    P.status = reinterpret_cast<unsigned *>(ws);
+    P.krot = reinterpret_cast<__nv_bfloat16 *>(ws + pl.krot_offset);
+    P.k_cache = static_cast<__nv_bfloat16 *>(k_cache);
+    P.v_cache = static_cast<__nv_bfloat16 *>(v_cache);
+    P.cap = k_cache ? cap : 0;
+    P.B = B;
+    P.T = T;
+    P.H = H;
+    P.Hkv = Hkv;
+    P.G = G;
+    P.kind = desc->kind;
+    P.window = desc->kind == SPARK_LAYER_SLIDING ? desc->window : 0;
+    P.gate_mode = desc->gate_mode;
+    P.rot_w = pl.rot_w;
+    P.n_qtiles = (T + tq - 1) / tq;
+    make_rope_table(desc, &P.rope);
+
+    const uint64_t heads = static_cast<uint64_t>(H + 2 * Hkv);
+    CUtensorMap tm_q, tm_kv_k, tm_kv_v, tm_krot, tm_out;
+    std::memset(&tm_krot, 0, sizeof(tm_krot));
+    {
+        // qkv as [B][T][heads][256]
+        const uint64_t dims[4] = {kHeadDim, heads, static_cast<uint64_t>(T),
+                                  static_cast<uint64_t>(B)};
+        const uint64_t strides[3] = {kHeadDim * 2ull, heads * kHeadDim * 2ull,
+                                     static_cast<uint64_t>(T) * heads * kHeadDim * 2ull};
+        const uint32_t box_q[4] = {64, static_cast<uint32_t>(G), static_cast<uint32_t>(tq), 1};
+        const uint32_t box_k[4] = {64, 1, 128, 1};
+        const uint32_t box_v[4] = {64, 1, 32, 1};
+        if (!encode_bf16(&tm_q, qkv, 4, dims, strides, box_q, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_bf16(&tm_kv_k, qkv, 4, dims, strides, box_k, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_bf16(&tm_kv_v, qkv, 4, dims, strides, box_v, CU_TENSOR_MAP_SWIZZLE_128B))
+            return SPARK_ERR_CUDA;
+    }
+    if (pl.rot_w > 0) {
+        // rotated K as [B*Hkv][T][rot_w]
+        const uint64_t dims[3] = {static_cast<uint64_t>(pl.rot_w), static_cast<uint64_t>(T),
+                                  static_cast<uint64_t>(B) * Hkv};
+        const uint64_t strides[2] = {pl.rot_w * 2ull,
+                                     static_cast<uint64_t>(T) * pl.rot_w * 2ull};
+        const uint32_t box[3] = {64, 128, 1};
+        if (!encode_bf16(&tm_krot, P.krot, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+            return SPARK_ERR_CUDA;
+    }
+    {
+        // out as [B][T][H][256]
+        const uint64_t dims[4] = {kHeadDim, static_cast<uint64_t>(H), static_cast<uint64_t>(T),
+                                  static_cast<uint64_t>(B)};
+        const uint64_t strides[3] = {kHeadDim * 2ull, static_cast<uint64_t>(H) * kHeadDim * 2ull,
+                                     static_cast<uint64_t>(T) * H * kHeadDim * 2ull};
+        const uint32_t box[4] = {64, static_cast<uint32_t>(G), static_cast<uint32_t>(tq), 1};
+        if (!encode_bf16(&tm_out, out, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+            return SPARK_ERR_CUDA;
+    }
+    return from_cuda(launch_prefill(tm_q, tm_kv_k, tm_kv_v, tm_krot, tm_out, P,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 }  // namespace spark
 
@@ -290,6 +381,7 @@ spark_status spark_attn_decode(const void *qkv, const float *gate, const int32_t
     P.G = H / Hkv;
     P.kind = desc->kind;
     P.window = desc->kind == SPARK_LAYER_SLIDING ? desc->window : 0;
+    P.gate_mode = desc->gate_mode;
     P.nsplit = pl.nsplit;
     P.chunk = pl.chunk;
     make_rope_table(desc, &P.rope);
@@ -313,82 +405,26 @@ size_t spark_attn_prefill_workspace_size(int B, int T, int H, int Hkv,
     return plan_prefill(B, T, Hkv, desc).bytes;
 }
 
-spark_status spark_attn_prefill(const void *qkv, const float *gate, const int32_t *pos,
-                                const spark_layer_desc *desc, int B, int T, int H, int Hkv,
-                                void *out, void *workspace, size_t workspace_bytes,
-                                void *stream) {
-    spark_status st = check_prefill(B, T, H, Hkv, desc);
+extern "C" spark_status spark_attn_prefill(const void *qkv, const float *gate, const int32_t *pos,
+                                           const spark_layer_desc *desc, int B, int T, int H,
+                                           int Hkv, void *out, void *workspace,
+                                           size_t workspace_bytes, void *stream) {
+    return prefill_impl(qkv, gate, pos, desc, B, T, H, Hkv, out, nullptr, nullptr, 0, workspace,
+                        workspace_bytes, stream);
+}
+
+extern "C" spark_status spark_attn_prefill_cache(const void *qkv, const float *gate,
+                                                 const int32_t *pos, void *k_cache,
+                                                 void *v_cache, int64_t cap,
+                                                 const spark_layer_desc *desc, int B, int T,
+                                                 int H, int Hkv, void *out, void *workspace,
+                                                 size_t workspace_bytes, void *stream) {
+    const spark_status st = check_prefill(B, T, H, Hkv, desc);
     if (st != SPARK_OK) return st;
     if (B == 0 || T == 0) return SPARK_OK;
-    if (!qkv || !gate || !pos || !out || !workspace) return SPARK_ERR_NULL;
-    if (!aligned(qkv, 16) || !aligned(out, 16) || !aligned(gate, 4) || !aligned(pos, 4) ||
-        !aligned(workspace, 256))
-        return SPARK_ERR_ALIGN;
-    const PrefillPlan pl = plan_prefill(B, T, Hkv, desc);
-    if (workspace_bytes < pl.bytes) return SPARK_ERR_WORKSPACE;
-    st = check_device();
-    if (st != SPARK_OK) return st;
-
-    const int G = H / Hkv;
-    const int tq = kPrefillRows / G;  // tokens per query tile
-    PrefillParams P;
-    std::memset(&P, 0, sizeof(P));
-    P.qkv = static_cast<const __nv_bfloat16 *>(qkv);
-    P.gate = gate;
-    P.pos = pos;
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-    P.status = reinterpret_cast<unsigned *>(ws);
-    P.krot = reinterpret_cast<__nv_bfloat16 *>(ws + pl.krot_offset);
-    P.B = B;
-    P.T = T;
-    P.H = H;
-    P.Hkv = Hkv;
-    P.G = G;
-    P.kind = desc->kind;
-    P.window = desc->kind == SPARK_LAYER_SLIDING ? desc->window : 0;
-    P.rot_w = pl.rot_w;
-    P.n_qtiles = (T + tq - 1) / tq;
-    make_rope_table(desc, &P.rope);
-
-    const uint64_t heads = static_cast<uint64_t>(H + 2 * Hkv);
-    CUtensorMap tm_q, tm_kv_k, tm_kv_v, tm_krot, tm_out;
-    std::memset(&tm_krot, 0, sizeof(tm_krot));
-    {
-        // qkv as [B][T][heads][256]
-        const uint64_t dims[4] = {kHeadDim, heads, static_cast<uint64_t>(T),
-                                  static_cast<uint64_t>(B)};
-        const uint64_t strides[3] = {kHeadDim * 2ull, heads * kHeadDim * 2ull,
-                                     static_cast<uint64_t>(T) * heads * kHeadDim * 2ull};
-        const uint32_t box_q[4] = {64, static_cast<uint32_t>(G), static_cast<uint32_t>(tq), 1};
-        const uint32_t box_k[4] = {64, 1, 128, 1};
-        const uint32_t box_v[4] = {64, 1, 32, 1};
-        if (!encode_bf16(&tm_q, qkv, 4, dims, strides, box_q, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_bf16(&tm_kv_k, qkv, 4, dims, strides, box_k, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_bf16(&tm_kv_v, qkv, 4, dims, strides, box_v, CU_TENSOR_MAP_SWIZZLE_128B))
-            return SPARK_ERR_CUDA;
-    }
-    if (pl.rot_w > 0) {
-        // rotated K as [B*Hkv][T][rot_w]
-        const uint64_t dims[3] = {static_cast<uint64_t>(pl.rot_w), static_cast<uint64_t>(T),
-                                  static_cast<uint64_t>(B) * Hkv};
-        const uint64_t strides[2] = {pl.rot_w * 2ull,
-                                     static_cast<uint64_t>(T) * pl.rot_w * 2ull};
-        const uint32_t box[3] = {64, 128, 1};
-        if (!encode_bf16(&tm_krot, P.krot, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
-            return SPARK_ERR_CUDA;
-    }
-    {
-        // out as [B][T][H][256]
-        const uint64_t dims[4] = {kHeadDim, static_cast<uint64_t>(H), static_cast<uint64_t>(T),
-                                  static_cast<uint64_t>(B)};
-        const uint64_t strides[3] = {kHeadDim * 2ull, static_cast<uint64_t>(H) * kHeadDim * 2ull,
-                                     static_cast<uint64_t>(T) * H * kHeadDim * 2ull};
-        const uint32_t box[4] = {64, static_cast<uint32_t>(G), static_cast<uint32_t>(tq), 1};
-        if (!encode_bf16(&tm_out, out, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
-            return SPARK_ERR_CUDA;
-    }
-    return from_cuda(launch_prefill(tm_q, tm_kv_k, tm_kv_v, tm_krot, tm_out, P,
-                                    static_cast<cudaStream_t>(stream)));
+    if (!k_cache || !v_cache) return SPARK_ERR_NULL;
+    return prefill_impl(qkv, gate, pos, desc, B, T, H, Hkv, out, k_cache, v_cache, cap,
+                        workspace, workspace_bytes, stream);
 }
 
 spark_status spark_attn_read_status(void *workspace, uint32_t *status_out, int clear,
@@ -501,6 +537,7 @@ extern "C" spark_status spark_attn_decode_noalloc(const void *qkv, const float *
     P.G = H / Hkv;
     P.kind = desc->kind;
     P.window = desc->kind == SPARK_LAYER_SLIDING ? desc->window : 0;
+    P.gate_mode = desc->gate_mode;
     P.nsplit = pl.nsplit;
     P.chunk = pl.chunk;
     make_rope_table(desc, &P.rope);

@@ -69,7 +69,7 @@ typedef enum spark_status {
     SPARK_ERR_NULL = 1,        /* a required pointer is NULL */
     SPARK_ERR_SHAPE = 2,       /* a size is negative or inconsistent (H % Hkv, window < 1, ...) */
     SPARK_ERR_UNSUPPORTED = 3, /* valid but not built: H/Hkv not in {1,2,4,8}, rot_dim not a
-                                  multiple of 16, gate_mode other than sigmoid */
+                                  multiple of 16, gate_mode other than sigmoid or silu */
     SPARK_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned (workspace: 256-byte) */
     SPARK_ERR_CAPACITY = 5,    /* a sliding ring smaller than its window, cap < 1 */
     SPARK_ERR_WORKSPACE = 6,   /* workspace NULL or smaller than the size query returns */
@@ -83,7 +83,8 @@ typedef enum spark_layer_kind {
 } spark_layer_kind;
 
 typedef enum spark_gate_mode {
-    SPARK_GATE_SIGMOID = 0     /* out *= 1 / (1 + exp(-gate_logit)) */
+    SPARK_GATE_SIGMOID = 0,    /* out *= 1 / (1 + exp(-g)), g = gate logit (released models) */
+    SPARK_GATE_SILU = 1        /* out *= g / (1 + exp(-g)) (gate_attn_act_mode = silu, §3) */
 } spark_gate_mode;
 
 /* Layer-type descriptor (the per-layer fields of the model config). */
@@ -121,6 +122,26 @@ spark_status spark_attn_prefill(const void *qkv, const float *gate, const int32_
                                 const spark_layer_desc *desc, int B, int T, int H, int Hkv,
                                 void *out, void *workspace, size_t workspace_bytes,
                                 void *stream);
+
+/*
+ * Prefill that also fills the decode cache: computes exactly what
+ * spark_attn_prefill computes and stores every token's rotated key (all 256
+ * dims) and value in the cache, as the model does while it prefills
+ * (past_key_values.update; Spark-X2.5-4B hybrid-attention explainer, lshu.cn).
+ *
+ *   k_cache, v_cache  bf16 [B, Hkv, cap, 256], written in place.
+ *            FULL: token t -> slot t, needs cap >= T.
+ *            SLIDING: ring, token t -> slot t mod cap, needs cap >= window;
+ *            only the last min(T, cap) tokens are stored (the others would be
+ *            overwritten within the same prefill).
+ *   Other arguments as for spark_attn_prefill (same workspace size).
+ * A spark_attn_decode at pos = T on the same caches continues the sequence.
+ */
+spark_status spark_attn_prefill_cache(const void *qkv, const float *gate, const int32_t *pos,
+                                      void *k_cache, void *v_cache, int64_t cap,
+                                      const spark_layer_desc *desc, int B, int T, int H, int Hkv,
+                                      void *out, void *workspace, size_t workspace_bytes,
+                                      void *stream);
 
 /*
  * Decode: one new token per sequence.

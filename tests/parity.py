@@ -43,3 +43,23 @@ def f64_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     u = f.view(np.uint32).astype(np.uint64)
     rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
     return rounded.astype(np.uint16)
+
+
+def bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> exact fp64 values."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def check_rotated_bf16(got_bits: np.ndarray, exact: np.ndarray, x_scale, what: str = ""):
+    """A RoPE output stored as bf16 against the exact fp64 rotation.
+
+    The GPU rotates in fp32 with angles good to ~2e-7 rad, then rounds to
+    bf16.  Where the two terms of a rotation nearly cancel the result is tiny
+    and those fp32 errors, small against the inputs, exceed one bf16 ulp of
+    the result; so the bound is one bf16 ulp of the value (2^-8 relative) plus
+    2e-6 of the input magnitude x_scale (per row, broadcastable)."""
+    got = bits_to_f64(got_bits)
+    bound = np.abs(exact) * 2.0 ** -8 + 2e-6 * np.asarray(x_scale, dtype=np.float64)
+    bad = np.abs(got - exact) > bound
+    assert not np.any(bad), f"{what}: {int(bad.sum())} rotated values off (first at {np.argwhere(bad)[0]})"

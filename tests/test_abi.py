@@ -73,7 +73,7 @@ def prefill_call(d=None, B=1, T=64, H=16, Hkv=4, ptrs=None, ws_bytes=1 << 30, nu
     (dict(d=desc(rot=258)), bnd.SPARK_ERR_SHAPE),
     (dict(d=desc(rot=8)), bnd.SPARK_ERR_UNSUPPORTED),
     (dict(d=desc(theta=0.0)), bnd.SPARK_ERR_SHAPE),
-    (dict(d=desc(gate=1)), bnd.SPARK_ERR_UNSUPPORTED),
+    (dict(d=desc(gate=2)), bnd.SPARK_ERR_UNSUPPORTED),
     (dict(d=desc(kind=2)), bnd.SPARK_ERR_SHAPE),
     (dict(cap=511), bnd.SPARK_ERR_CAPACITY),                 # ring smaller than the window
     (dict(cap=0, d=desc(kind=0, window=0, theta=5e6, rot=64)), bnd.SPARK_ERR_CAPACITY),

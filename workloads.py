@@ -41,7 +41,7 @@ class Layer:
     window: int
     theta: float
     rot_dim: int
-    gate_mode: int = 0  # 0 = sigmoid (the only mode the released checkpoints use)
+    gate_mode: int = 0  # 0 = sigmoid (the released checkpoints), 1 = silu
 
 
 # Layered RoPE table (§4) and window (§1) of the Spark-X2.5 architecture page.
