@@ -188,6 +188,26 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             mma_bf16_16816(sc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
         }
 
+        // Slots past the chunk end may hold anything (even NaN bit patterns in
+        // a cache that was never written there); their probabilities are 0,
+        // but 0 * NaN is NaN in P*V, so this warp zeroes its V rows past the end.
+        {
+            const long long row0 = c_lo + static_cast<long long>(t) * kDecTile + warp * 16;
+            if (row0 + 16 > c_hi) {
+                uint8_t *vrows = stages + s * kDecStageBytes + kDecTileBytes;
+                for (int rr = 0; rr < 16; ++rr) {
+                    if (row0 + rr < c_hi) continue;
+                    const int vr = warp * 16 + rr;  // 4 chunks of 128 bytes per row
+                    *reinterpret_cast<uint4 *>(vrows + (lane >> 3) * (kDecTileBytes / 4) +
+                                               vr * 128 + (lane & 7) * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
+                // the stage is refilled by TMA later: order these writes first
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+        }
+
         // this thread's two slots (rows lane/4 and lane/4 + 8) and two heads
         const long long sa = c_lo + static_cast<long long>(t) * kDecTile + warp * 16 + (lane >> 2);
         const long long sb = sa + 8;

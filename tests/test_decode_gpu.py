@@ -126,6 +126,29 @@ def test_split_count_invariance(cuda):
         assert torch.allclose(o, outs[0], atol=8e-3, rtol=0)
 
 
+def test_unwritten_slots_may_hold_nan(cuda):
+    """Cache slots at and past the new position were never written and may hold
+    any bit pattern; NaN there must not reach the output."""
+    layer = wl.FULL_LAYER
+    B, H, Hkv, cap = 2, 16, 4, 1000
+    case = wl.DecodeCase("t", B=B, H=H, Hkv=Hkv, layer=layer, seed=12, cap=cap, len_lo=0,
+                         len_hi=0)
+    step = wl.make_decode_step_inputs(case)
+    pos = torch.tensor([100, 777], dtype=torch.int32)
+    kc = wl.fill_cache_(torch.empty((B, Hkv, cap, 256), dtype=torch.bfloat16), 13)
+    vc = wl.fill_cache_(torch.empty_like(kc), 14)
+    for b, p in enumerate(pos.tolist()):
+        kc[b, :, p:] = float("nan")
+        vc[b, :, p:] = float("nan")
+    kd, vd = kc.to(cuda), vc.to(cuda)
+    out = fga.spark_attn_decode(step["qkv"].to(cuda), step["gate"].to(cuda), pos.to(cuda), kd, vd,
+                                layer)
+    want, _, _ = oracle.decode(wl.bf16_bits(step["qkv"]), step["gate"].numpy(), pos.numpy(),
+                               wl.bf16_bits(kc), wl.bf16_bits(vc), layer.kind, layer.window,
+                               layer.theta, layer.rot_dim, H, Hkv)
+    check_close(out, want, "decode over NaN-poisoned unwritten slots")
+
+
 def test_bad_position_is_flagged(cuda):
     """A full-layer position at or past the cache end is skipped and flagged;
     the other sequences are still computed."""
