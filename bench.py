@@ -430,11 +430,11 @@ def run_ours(args, rank, world, local):
 # Per-launch DRAM traffic (read + write bytes) from ncu captures of the
 # current kernels, scaled to one launch of the bench workload; None when the
 # kernels changed since the counters were taken.
-# decode_split_kernel: 540.5 MB in a 131,072-token capture, scaled x8 to the
+# decode_split_kernel: 540.0 MB in a 131,072-token capture, scaled x8 to the
 # 1,048,576-token layer; prefill_attn_kernel: 491.1 MB measured on this workload.
 TRAFFIC: dict[str, float | None] = {
-    "decode_split_kernel": 540.546048e6 * 8,
-    "prefill_attn_kernel": 491.14496e6,
+    "decode_split_kernel": 539.981056e6 * 8,
+    "prefill_attn_kernel": 491.147776e6,
 }
 
 
