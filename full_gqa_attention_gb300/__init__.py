@@ -23,6 +23,7 @@ from ._binding import (  # noqa: F401
     spark_attn_decode_workspace_size,
     spark_attn_prefill,
     spark_attn_prefill_cache,
+    spark_attn_prefill_chunk,
     spark_attn_prefill_workspace_size,
     spark_attn_read_status,
     spark_attn_version,

@@ -59,6 +59,9 @@ def _load() -> ctypes.CDLL:
     lib.spark_attn_prefill_cache.argtypes = [P, P, P, P, P, i64, D, i32, i32, i32, i32, P, P,
                                              sz, P]
     lib.spark_attn_prefill_cache.restype = i32
+    lib.spark_attn_prefill_chunk.argtypes = [P, P, P, P, P, i64, P, D, i32, i32, i32, i32, P, P,
+                                             sz, P]
+    lib.spark_attn_prefill_chunk.restype = i32
     lib.spark_attn_decode_workspace_size.argtypes = [i32, i32, i32, i64, D]
     lib.spark_attn_decode_workspace_size.restype = sz
     lib.spark_attn_decode.argtypes = [P, P, P, P, P, i64, D, i32, i32, i32, P, P, sz, P]
@@ -195,6 +198,41 @@ def spark_attn_prefill_cache(qkv: torch.Tensor, gate: torch.Tensor, pos: torch.T
                                       _stream(stream))
     if st != SPARK_OK:
         raise SparkError(st, "spark_attn_prefill_cache")
+    return out
+
+
+def spark_attn_prefill_chunk(qkv: torch.Tensor, gate: torch.Tensor, pos: torch.Tensor,
+                             k_cache: torch.Tensor, v_cache: torch.Tensor, start: torch.Tensor,
+                             layer, out: torch.Tensor | None = None,
+                             workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Chunked prefill: T more tokens per sequence on top of start[b] cached
+    tokens (start: CUDA int32 [B]); see the C header for the cache rules."""
+    _need(qkv, torch.bfloat16, "qkv")
+    _need(gate, torch.float32, "gate")
+    _need(pos, torch.int32, "pos")
+    _need(k_cache, torch.bfloat16, "k_cache")
+    _need(v_cache, torch.bfloat16, "v_cache")
+    _need(start, torch.int32, "start")
+    B, T, W = qkv.shape
+    H = gate.shape[-1]
+    Hkv = (W // HEAD_DIM - H) // 2
+    if (gate.shape != (B, T, H) or pos.shape != (B, T) or (H + 2 * Hkv) * HEAD_DIM != W
+            or start.shape != (B,) or k_cache.shape != v_cache.shape
+            or k_cache.shape[:2] != (B, Hkv) or k_cache.shape[3] != HEAD_DIM):
+        raise ValueError("inconsistent chunked-prefill shapes")
+    d = as_desc(layer)
+    if out is None:
+        out = torch.empty((B, T, H * HEAD_DIM), dtype=torch.bfloat16, device=qkv.device)
+    _need(out, torch.bfloat16, "out")
+    need = lib.spark_attn_prefill_workspace_size(B, T, H, Hkv, ctypes.byref(d))
+    if workspace is None:
+        workspace = new_workspace(need, qkv.device)
+    st = lib.spark_attn_prefill_chunk(_ptr(qkv), _ptr(gate), _ptr(pos), _ptr(k_cache),
+                                      _ptr(v_cache), k_cache.shape[2], _ptr(start),
+                                      ctypes.byref(d), B, T, H, Hkv, _ptr(out), _ptr(workspace),
+                                      workspace.numel(), _stream(stream))
+    if st != SPARK_OK:
+        raise SparkError(st, "spark_attn_prefill_chunk")
     return out
 
 

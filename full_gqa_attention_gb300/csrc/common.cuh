@@ -117,6 +117,8 @@ struct PrefillParams {
     __nv_bfloat16 *k_cache;    // optional [B, Hkv, cap, 256]: receives rotated K
     __nv_bfloat16 *v_cache;    // optional [B, Hkv, cap, 256]: receives V
     long long cap;             // cache slots (when k_cache is set)
+    const int32_t *start;      // optional [B]: tokens cached before this chunk (chunked
+                               // prefill: queries and keys are then at start + t)
     unsigned *status;
     int B, T, H, Hkv, G;
     int kind, window;

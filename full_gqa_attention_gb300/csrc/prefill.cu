@@ -107,7 +107,12 @@ __global__ void __launch_bounds__(kRopeThreads) prefill_store_kv_kernel(
     if (row >= static_cast<long long>(P.B) * P.T) return;
     const int b = static_cast<int>(row / P.T), t = static_cast<int>(row % P.T);
     if (P.kind == kLayerSliding && t < P.T - P.cap) return;  // overwritten later in the ring
-    const long long slot = (P.kind == kLayerFull) ? t : t % P.cap;
+    const long long a = (P.start ? static_cast<long long>(P.start[b]) : 0) + t;  // absolute index
+    if (a < 0 || (P.kind == kLayerFull && a >= P.cap)) {
+        if (it == 0 && t == 0) atomicOr(P.status, kErrPosition);
+        return;
+    }
+    const long long slot = (P.kind == kLayerFull) ? a : a % P.cap;
     const size_t width = static_cast<size_t>(P.H + 2 * P.Hkv) * kHeadDim;
     const __nv_bfloat16 *src_k = P.qkv + row * width + static_cast<size_t>(P.H) * kHeadDim;
     const __nv_bfloat16 *src_v = src_k + static_cast<size_t>(P.Hkv) * kHeadDim;
@@ -147,6 +152,31 @@ __global__ void __launch_bounds__(kRopeThreads) prefill_store_kv_kernel(
         for (int g = 0; g < P.Hkv; ++g)
             *reinterpret_cast<uint4 *>(P.v_cache + base + g * head_stride + d0) =
                 *reinterpret_cast<const uint4 *>(src_v + g * kHeadDim + d0);
+    }
+}
+
+// Zeroes the cache slots that the last key tile of a chunked prefill may read
+// past the chunk end but that no token has written yet (a full layer's future
+// slots, or ring slots on the first pass): their probabilities are 0, but a
+// never-written slot may hold NaN bit patterns and 0 * NaN is NaN in P*V.
+// One block per sequence.
+__global__ void __launch_bounds__(kRopeThreads) cache_zero_tail_kernel(
+    const __grid_constant__ PrefillParams P) {
+    grid_dep_wait();
+    grid_dep_launch();
+    const int b = blockIdx.x;
+    if (P.start[b] < 0) return;  // flagged by the store kernel
+    const long long a_end = static_cast<long long>(P.start[b]) + P.T;
+    const long long a_stop = (a_end + 127) / 128 * 128;
+    const long long last = a_stop < P.cap ? a_stop : P.cap;  // slots a_end..last-1
+    const int per_slot = P.Hkv * (kHeadDim / 8);             // 16-byte words per slot and tensor
+    for (long long w = threadIdx.x; w < (last - a_end) * per_slot; w += blockDim.x) {
+        const long long j = a_end + w / per_slot;
+        const int g = static_cast<int>((w % per_slot) / (kHeadDim / 8));
+        const int d0 = static_cast<int>(w % (kHeadDim / 8)) * 8;
+        const size_t off = ((static_cast<size_t>(b) * P.Hkv + g) * P.cap + j) * kHeadDim + d0;
+        *reinterpret_cast<uint4 *>(P.k_cache + off) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(P.v_cache + off) = make_uint4(0, 0, 0, 0);
     }
 }
 
@@ -231,6 +261,10 @@ __device__ __forceinline__ void named_bar(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
+// kFromCache: chunked prefill.  Queries are chunk tokens at absolute index
+// start[b] + t, keys are read from the KV cache (which already holds this
+// chunk's keys and values) and tm_kv_k / tm_kv_v then map the caches.
+template <bool kFromCache>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_kv_k,
@@ -257,9 +291,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int g = rem % P.Hkv, b = rem / P.Hkv;
     const int t0 = qtile * tq;
     const int t_end = (t0 + tq < P.T) ? t0 + tq : P.T;  // exclusive
-    const int kv_lo = (P.kind == kLayerFull) ? 0 : (t0 - P.window + 1 > 0 ? t0 - P.window + 1 : 0);
-    const int kv_hi = t_end;
-    const int ntiles = (kv_hi - kv_lo + kBN - 1) / kBN;
 
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i) {
@@ -289,10 +320,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t tmem = tmem_base_sh;
     grid_dep_wait();  // rotated K (previous kernel) and every input are ready
 
+    // Absolute indices: queries t0..t_end-1 of the chunk sit at start + t.
+    int start = 0;
+    bool skip = false;
+    if constexpr (kFromCache) {
+        start = P.start[b];
+        skip = start < 0 || (P.kind == kLayerFull && static_cast<long long>(start) + P.T > P.cap);
+        if (skip && tid == 0 && qtile == P.n_qtiles - 1 && g == 0) atomicOr(P.status, kErrPosition);
+    }
+    const int a0 = start + t0;
+    int kv_lo = (P.kind == kLayerFull) ? 0 : (a0 - P.window + 1 > 0 ? a0 - P.window + 1 : 0);
+    // a ring is read in 128-key tiles aligned to its 128-slot boundaries, so
+    // that no tile wraps around the end of the ring
+    if (kFromCache && P.kind == kLayerSliding) kv_lo &= ~(kBN - 1);
+    const int kv_hi = start + t_end;
+    const int ntiles = skip ? 0 : (kv_hi - kv_lo + kBN - 1) / kBN;
+
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         int sc = 0;  // ring slots filled so far
-        if (lane == 0) {
+        if (lane == 0 && !skip) {
             mbar_arrive_expect_tx(&bars[kBarQFull], kQBytes);
 #pragma unroll
             for (int c = 0; c < 4; ++c)
@@ -313,12 +360,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     int slot;
                     if (!next_slot(slot)) return false;
                     uint8_t *dst = ring + slot * kSlotBytes;
-                    if (c * 64 < P.rot_w)
+                    if constexpr (kFromCache) {
+                        const int slot0 = (P.kind == kLayerSliding)
+                                              ? static_cast<int>(key0 % P.cap) : key0;
+                        tma_load_4d(dst, &tm_kv_k, &bars[kBarSlotFull + slot], c * 64, slot0, g,
+                                    b);
+                    } else if (c * 64 < P.rot_w) {
                         tma_load_3d(dst, &tm_krot, &bars[kBarSlotFull + slot], c * 64, key0,
                                     b * P.Hkv + g);
-                    else
+                    } else {
                         tma_load_4d(dst, &tm_kv_k, &bars[kBarSlotFull + slot], c * 64, P.H + g,
                                     key0, b);
+                    }
                     ++sc;
                 }
                 return true;
@@ -329,11 +382,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     int slot;
                     if (!next_slot(slot)) return false;
                     uint8_t *dst = ring + slot * kSlotBytes;
+                    if constexpr (kFromCache) {
+                        const int slot0 = (P.kind == kLayerSliding)
+                                              ? static_cast<int>(key0 % P.cap) : key0;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        tma_load_4d(dst + c * (kSlotBytes / 4), &tm_kv_v,
-                                    &bars[kBarSlotFull + slot], c * 64, P.H + P.Hkv + g,
-                                    key0 + vs * 32, b);
+                        for (int c = 0; c < 4; ++c)
+                            tma_load_4d(dst + c * (kSlotBytes / 4), &tm_kv_v,
+                                        &bars[kBarSlotFull + slot], c * 64, slot0 + vs * 32, g, b);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            tma_load_4d(dst + c * (kSlotBytes / 4), &tm_kv_v,
+                                        &bars[kBarSlotFull + slot], c * 64, P.H + P.Hkv + g,
+                                        key0 + vs * 32, b);
+                    }
                     ++sc;
                 }
                 return true;
@@ -357,7 +419,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && !skip) {
             int sc = 0;
             const uint32_t q_addr = smem_u32(qbuf);
             const uint32_t ring_addr = smem_u32(ring);
@@ -446,12 +508,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int sth = tid - kSoftmaxWarp0 * 32;       // 0..255 among softmax threads
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const int tok = t0 + row / G;
+        const int tok_abs = start + tok;                // absolute index for the mask
         const int head = g * G + row % G;
         const bool valid = tok < P.T;
         const size_t trow = static_cast<size_t>(b) * P.T + (valid ? tok : 0);
         const int p = valid ? P.pos[trow] : 0;
         const float gate_logit = valid ? P.gate[trow * P.H + head] : 0.f;
-        bool ok = mbar_wait(&bars[kBarQFull], 0, &abort_flag, P.status);
+        bool ok = !skip && mbar_wait(&bars[kBarQFull], 0, &abort_flag, P.status);
 
         // rotate this row of Q in place (bf16 in, fp32 math, bf16 out); the
         // two warpgroups take alternate groups of 8 pairs, and the G rows of a
@@ -465,14 +528,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
         }
         fence_proxy_async_smem();
-        mbar_arrive(&bars[kBarQReady]);
+        if (!skip) mbar_arrive(&bars[kBarQReady]);
 
         // Scores stay in raw units s = q.k; probabilities are
         // exp2(s * kScaleLog2 - m * kScaleLog2) with m the row's reference max.
         // The reference moves only when the row max grows past it by the
         // raw equivalent of 2^8.
         constexpr float kLazyRaw = 8.0f / kScaleLog2;
-        const int t_last = t_end - 1;
+        const int a_last = start + t_end - 1;
         const int col0 = wg * 64;                       // first score column of this thread
         float m_run = -INFINITY, l_part = 0.f;
         for (int j = 0; ok && j < ntiles; ++j) {
@@ -488,13 +551,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
             for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(sv[c]);
             const int key0 = kv_lo + j * kBN;
-            const bool need_mask = (key0 + kBN - 1 > t0) ||
-                                   (P.kind == kLayerSliding && t_last - key0 >= P.window);
+            const bool need_mask = (key0 + kBN - 1 > a0) ||
+                                   (P.kind == kLayerSliding && a_last - key0 >= P.window);
             if (need_mask) {
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
                     const int key = key0 + col0 + c;
-                    const bool vis = key <= tok && (P.kind == kLayerFull || tok - key < P.window);
+                    const bool vis =
+                        key <= tok_abs && (P.kind == kLayerFull || tok_abs - key < P.window);
                     x[c] = vis ? x[c] : -INFINITY;
                 }
             }
@@ -557,6 +621,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // epilogue: O / l * sigmoid(gate) -> bf16 -> staged in the Q buffer -> TMA store
         if (sth == 0) grid_dep_launch();
         if (ok) ok = mbar_wait(&bars[kBarOFinal], 0, &abort_flag, P.status);
+        if (skip) ok = false;
         red_l[wg][row] = l_part;
         named_bar(1, kSoftmaxThreads);
         {
@@ -585,7 +650,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             fence_proxy_async_smem();
             named_bar(1, kSoftmaxThreads);
-            if (sth == 0 && !abort_flag) {
+            if (sth == 0 && !abort_flag && !skip) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
                     tma_store_4d(&tm_out, qbuf + c * kSlotBytes, c * 64, g * G, t0, b);
@@ -607,30 +672,45 @@ cudaError_t launch_prefill(const CUtensorMap &tm_q, const CUtensorMap &tm_kv_k,
                            const CUtensorMap &tm_kv_v, const CUtensorMap &tm_krot,
                            const CUtensorMap &tm_out, const PrefillParams &P,
                            cudaStream_t stream) {
+    const int r = P.rope.rot_dim;
+    const long long store_items = r / 16 + (kHeadDim - r) / 8 + kHeadDim / 8;
+    const long long store_blocks =
+        (static_cast<long long>(P.B) * P.T * store_items + kRopeThreads - 1) / kRopeThreads;
+    const unsigned grid = static_cast<unsigned>(P.n_qtiles) * P.Hkv * P.B;
+    cudaError_t err;
+    if (P.start != nullptr) {
+        // chunked prefill: store the chunk's keys and values first, clear the
+        // never-written slots the last key tile may read, then attend over
+        // the cache
+        err = launch_overlapped(prefill_store_kv_kernel, dim3(static_cast<unsigned>(store_blocks)),
+                                dim3(kRopeThreads), 0, stream, P);
+        if (err != cudaSuccess) return err;
+        err = launch_overlapped(cache_zero_tail_kernel, dim3(P.B), dim3(kRopeThreads), 0, stream,
+                                P);
+        if (err != cudaSuccess) return err;
+        err = cudaFuncSetAttribute(prefill_attn_kernel<true>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmemBytes);
+        if (err != cudaSuccess) return err;
+        return launch_overlapped(prefill_attn_kernel<true>, dim3(grid), dim3(kAttnThreads),
+                                 kAttnSmemBytes, stream, tm_q, tm_kv_k, tm_kv_v, tm_krot, tm_out,
+                                 P);
+    }
     if (P.rot_w > 0) {
-        const int r = P.rope.rot_dim;
         const long long items = r / 16 + (P.rot_w - r) / 8;
         const long long threads = static_cast<long long>(P.B) * P.T * items;
         const long long blocks = (threads + kRopeThreads - 1) / kRopeThreads;
-        cudaError_t err = launch_overlapped(prefill_rope_k_kernel,
-                                            dim3(static_cast<unsigned>(blocks)),
-                                            dim3(kRopeThreads), 0, stream, P);
+        err = launch_overlapped(prefill_rope_k_kernel, dim3(static_cast<unsigned>(blocks)),
+                                dim3(kRopeThreads), 0, stream, P);
         if (err != cudaSuccess) return err;
     }
-    cudaError_t err = cudaFuncSetAttribute(prefill_attn_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           kAttnSmemBytes);
+    err = cudaFuncSetAttribute(prefill_attn_kernel<false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmemBytes);
     if (err != cudaSuccess) return err;
-    const unsigned grid = static_cast<unsigned>(P.n_qtiles) * P.Hkv * P.B;
-    err = launch_overlapped(prefill_attn_kernel, dim3(grid), dim3(kAttnThreads), kAttnSmemBytes,
-                            stream, tm_q, tm_kv_k, tm_kv_v, tm_krot, tm_out, P);
+    err = launch_overlapped(prefill_attn_kernel<false>, dim3(grid), dim3(kAttnThreads),
+                            kAttnSmemBytes, stream, tm_q, tm_kv_k, tm_kv_v, tm_krot, tm_out, P);
     if (err != cudaSuccess || P.k_cache == nullptr) return err;
     // fill the decode cache (it reads only qkv and pos)
-    const int r = P.rope.rot_dim;
-    const long long items = r / 16 + (kHeadDim - r) / 8 + kHeadDim / 8;
-    const long long threads = static_cast<long long>(P.B) * P.T * items;
-    const long long blocks = (threads + kRopeThreads - 1) / kRopeThreads;
-    return launch_overlapped(prefill_store_kv_kernel, dim3(static_cast<unsigned>(blocks)),
+    return launch_overlapped(prefill_store_kv_kernel, dim3(static_cast<unsigned>(store_blocks)),
                              dim3(kRopeThreads), 0, stream, P);
 }
 

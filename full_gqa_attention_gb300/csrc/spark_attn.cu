@@ -226,11 +226,12 @@ spark_status check_prefill(int B, int T, int H, int Hkv, const spark_layer_desc 
     return SPARK_OK;
 }
 
-// Prefill, optionally filling the decode cache (k_cache != nullptr).
+// Prefill, optionally filling the decode cache (k_cache != nullptr), or a
+// chunked prefill over a cache that already holds start[b] tokens.
 spark_status prefill_impl(const void *qkv, const float *gate, const int32_t *pos,
                           const spark_layer_desc *desc, int B, int T, int H, int Hkv, void *out,
-                          void *k_cache, void *v_cache, int64_t cap, void *workspace,
-                          size_t workspace_bytes, void *stream) {
+                          void *k_cache, void *v_cache, int64_t cap, const int32_t *start,
+                          void *workspace, size_t workspace_bytes, void *stream) {
     spark_status st = check_prefill(B, T, H, Hkv, desc);
     if (st != SPARK_OK) return st;
     if (k_cache || v_cache) {
@@ -238,12 +239,18 @@ spark_status prefill_impl(const void *qkv, const float *gate, const int32_t *pos
         if (desc->kind == SPARK_LAYER_FULL && cap < T) return SPARK_ERR_CAPACITY;
         if (desc->kind == SPARK_LAYER_SLIDING && cap < desc->window) return SPARK_ERR_CAPACITY;
         if (cap > 0x7fffffffLL) return SPARK_ERR_UNSUPPORTED;
+        if (start && desc->kind == SPARK_LAYER_SLIDING) {
+            // the chunk's writes must not overwrite keys its own rows still see
+            if (cap < static_cast<int64_t>(desc->window) + T - 1) return SPARK_ERR_CAPACITY;
+            if (cap % 128 != 0) return SPARK_ERR_UNSUPPORTED;
+        }
     }
     if (B == 0 || T == 0) return SPARK_OK;
     if (!qkv || !gate || !pos || !out || !workspace) return SPARK_ERR_NULL;
     if ((k_cache == nullptr) != (v_cache == nullptr)) return SPARK_ERR_NULL;
     if (!aligned(qkv, 16) || !aligned(out, 16) || !aligned(gate, 4) || !aligned(pos, 4) ||
-        !aligned(workspace, 256) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        !aligned(workspace, 256) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(start, 4))
         return SPARK_ERR_ALIGN;
     const PrefillPlan pl = plan_prefill(B, T, Hkv, desc);
     if (workspace_bytes < pl.bytes) return SPARK_ERR_WORKSPACE;
@@ -263,6 +270,7 @@ spark_status prefill_impl(const void *qkv, const float *gate, const int32_t *pos
     P.k_cache = static_cast<__nv_bfloat16 *>(k_cache);
     P.v_cache = static_cast<__nv_bfloat16 *>(v_cache);
     P.cap = k_cache ? cap : 0;
+    P.start = start;
     P.B = B;
     P.T = T;
     P.H = H;
@@ -287,10 +295,28 @@ spark_status prefill_impl(const void *qkv, const float *gate, const int32_t *pos
         const uint32_t box_q[4] = {64, static_cast<uint32_t>(G), static_cast<uint32_t>(tq), 1};
         const uint32_t box_k[4] = {64, 1, 128, 1};
         const uint32_t box_v[4] = {64, 1, 32, 1};
-        if (!encode_bf16(&tm_q, qkv, 4, dims, strides, box_q, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_bf16(&tm_kv_k, qkv, 4, dims, strides, box_k, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_bf16(&tm_kv_v, qkv, 4, dims, strides, box_v, CU_TENSOR_MAP_SWIZZLE_128B))
+        if (!encode_bf16(&tm_q, qkv, 4, dims, strides, box_q, CU_TENSOR_MAP_SWIZZLE_128B))
             return SPARK_ERR_CUDA;
+        if (start) {
+            // chunked prefill: keys and values come from the caches [B][Hkv][cap][256]
+            const uint64_t cdims[4] = {kHeadDim, static_cast<uint64_t>(cap),
+                                       static_cast<uint64_t>(Hkv), static_cast<uint64_t>(B)};
+            const uint64_t cstrides[3] = {kHeadDim * 2ull,
+                                          static_cast<uint64_t>(cap) * kHeadDim * 2ull,
+                                          static_cast<uint64_t>(Hkv) * cap * kHeadDim * 2ull};
+            const uint32_t cbox_k[4] = {64, 128, 1, 1};
+            const uint32_t cbox_v[4] = {64, 32, 1, 1};
+            if (!encode_bf16(&tm_kv_k, k_cache, 4, cdims, cstrides, cbox_k,
+                             CU_TENSOR_MAP_SWIZZLE_128B) ||
+                !encode_bf16(&tm_kv_v, v_cache, 4, cdims, cstrides, cbox_v,
+                             CU_TENSOR_MAP_SWIZZLE_128B))
+                return SPARK_ERR_CUDA;
+        } else if (!encode_bf16(&tm_kv_k, qkv, 4, dims, strides, box_k,
+                                CU_TENSOR_MAP_SWIZZLE_128B) ||
+                   !encode_bf16(&tm_kv_v, qkv, 4, dims, strides, box_v,
+                                CU_TENSOR_MAP_SWIZZLE_128B)) {
+            return SPARK_ERR_CUDA;
+        }
     }
     if (pl.rot_w > 0) {
         // rotated K as [B*Hkv][T][rot_w]
@@ -409,8 +435,8 @@ extern "C" spark_status spark_attn_prefill(const void *qkv, const float *gate, c
                                            const spark_layer_desc *desc, int B, int T, int H,
                                            int Hkv, void *out, void *workspace,
                                            size_t workspace_bytes, void *stream) {
-    return prefill_impl(qkv, gate, pos, desc, B, T, H, Hkv, out, nullptr, nullptr, 0, workspace,
-                        workspace_bytes, stream);
+    return prefill_impl(qkv, gate, pos, desc, B, T, H, Hkv, out, nullptr, nullptr, 0, nullptr,
+                        workspace, workspace_bytes, stream);
 }
 
 extern "C" spark_status spark_attn_prefill_cache(const void *qkv, const float *gate,
@@ -423,7 +449,22 @@ extern "C" spark_status spark_attn_prefill_cache(const void *qkv, const float *g
     if (st != SPARK_OK) return st;
     if (B == 0 || T == 0) return SPARK_OK;
     if (!k_cache || !v_cache) return SPARK_ERR_NULL;
-    return prefill_impl(qkv, gate, pos, desc, B, T, H, Hkv, out, k_cache, v_cache, cap,
+    return prefill_impl(qkv, gate, pos, desc, B, T, H, Hkv, out, k_cache, v_cache, cap, nullptr,
+                        workspace, workspace_bytes, stream);
+}
+
+extern "C" spark_status spark_attn_prefill_chunk(const void *qkv, const float *gate,
+                                                 const int32_t *pos, void *k_cache,
+                                                 void *v_cache, int64_t cap,
+                                                 const int32_t *start,
+                                                 const spark_layer_desc *desc, int B, int T,
+                                                 int H, int Hkv, void *out, void *workspace,
+                                                 size_t workspace_bytes, void *stream) {
+    const spark_status st = check_prefill(B, T, H, Hkv, desc);
+    if (st != SPARK_OK) return st;
+    if (B == 0 || T == 0) return SPARK_OK;
+    if (!k_cache || !v_cache || !start) return SPARK_ERR_NULL;
+    return prefill_impl(qkv, gate, pos, desc, B, T, H, Hkv, out, k_cache, v_cache, cap, start,
                         workspace, workspace_bytes, stream);
 }
 

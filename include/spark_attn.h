@@ -144,6 +144,34 @@ spark_status spark_attn_prefill_cache(const void *qkv, const float *gate, const 
                                       void *stream);
 
 /*
+ * Chunked prefill: T more tokens per sequence on top of a cache that already
+ * holds the sequence's first start[b] tokens (as spark_attn_prefill_cache or
+ * earlier chunks left it).  Query token t of the chunk sits at index
+ * start[b] + t; it attends to every cached key and to the chunk's keys under
+ * the layer's mask on those indices.  The chunk's rotated keys and values are
+ * stored in the cache first (as spark_attn_prefill_cache stores them), so the
+ * next chunk or a spark_attn_decode at pos = start[b] + T continues the
+ * sequence.
+ *
+ *   start    int32 [B] (device): tokens already cached per sequence
+ *   k_cache, v_cache  bf16 [B, Hkv, cap, 256], updated in place.
+ *            FULL: needs start[b] + T <= cap (checked on the device: a
+ *            sequence past the end is skipped and SPARK_DEVERR_POSITION set).
+ *            SLIDING: a ring with cap >= window + T - 1 (so the chunk's writes
+ *            never replace keys its own rows still see) and cap a multiple of
+ *            128.
+ *   pos      RoPE positions of the chunk's tokens (normally start[b] + t).
+ *   Other arguments as for spark_attn_prefill (same workspace size).
+ * Cache slots past the chunk that were never written may hold anything; the
+ * call clears the few it reads.
+ */
+spark_status spark_attn_prefill_chunk(const void *qkv, const float *gate, const int32_t *pos,
+                                      void *k_cache, void *v_cache, int64_t cap,
+                                      const int32_t *start, const spark_layer_desc *desc, int B,
+                                      int T, int H, int Hkv, void *out, void *workspace,
+                                      size_t workspace_bytes, void *stream);
+
+/*
  * Decode: one new token per sequence.
  *
  *   qkv      bf16 [B, (H + 2*Hkv) * 256]   the new token's fused projection

@@ -75,3 +75,69 @@ def test_prefill_cache_rejects_small_cache(cuda):
     with pytest.raises(fga.SparkError) as e:
         fga.spark_attn_prefill_cache(q, g, p, kc, kc.clone(), layer)
     assert e.value.status == 5  # SPARK_ERR_CAPACITY: a full layer needs cap >= T
+
+
+@pytest.mark.parametrize("kind,T,cap,poison", [(FULL, 200, 2048, False), (FULL, 333, 1100, True),
+                                               (SLIDING, 200, 768, False),
+                                               (SLIDING, 129, 768, True)])
+def test_chunked_prefill(cuda, kind, T, cap, poison):
+    """Two sequences with 300 and 700 tokens already cached take a chunk of T
+    more tokens in one call (ragged start); the chunk's rows equal the oracle's
+    rows of a prefill over the whole sequence, and a decode of the next token
+    continues it.  With `poison`, slots never written hold NaN."""
+    layer = wl.FULL_LAYER if kind == FULL else wl.SLIDING_LAYER
+    H, Hkv = 16, 4
+    starts = [300, 700]
+    total = max(starts) + T + 1
+    case = wl.PrefillCase("chunk", B=2, T=total, H=H, Hkv=Hkv, layer=layer, seed=T + cap)
+    x = wl.make_prefill_inputs(case)
+    qkv, gate, pos = x["qkv"], x["gate"], x["pos"]
+    fill = float("nan") if poison else 0.0
+    kc = torch.full((2, Hkv, cap, 256), fill, dtype=torch.bfloat16, device=cuda)
+    vc = torch.full_like(kc, fill)
+    # cache the first start[b] tokens of each sequence
+    for b, s0 in enumerate(starts):
+        fga.spark_attn_prefill_cache(qkv[b:b + 1, :s0].contiguous().to(cuda),
+                                     gate[b:b + 1, :s0].contiguous().to(cuda),
+                                     pos[b:b + 1, :s0].contiguous().to(cuda),
+                                     kc[b:b + 1], vc[b:b + 1], layer)
+    # one chunk of T tokens for both sequences, at their own offsets
+    cq = torch.stack([qkv[b, s0:s0 + T] for b, s0 in enumerate(starts)]).contiguous()
+    cg = torch.stack([gate[b, s0:s0 + T] for b, s0 in enumerate(starts)]).contiguous()
+    cp = torch.stack([pos[b, s0:s0 + T] for b, s0 in enumerate(starts)]).contiguous()
+    start = torch.tensor(starts, dtype=torch.int32, device=cuda)
+    ws = fga.new_workspace(fga.spark_attn_prefill_workspace_size(2, T, H, Hkv, layer))
+    out = fga.spark_attn_prefill_chunk(cq.to(cuda), cg.to(cuda), cp.to(cuda), kc, vc, start,
+                                       layer, workspace=ws)
+    assert fga.spark_attn_read_status(ws) == 0
+    qb = wl.bf16_bits(qkv)
+    L = layer
+    for b, s0 in enumerate(starts):
+        rows = np.arange(s0, s0 + T, dtype=np.int64)
+        want = oracle.prefill(qb[b:b + 1, :s0 + T], gate[b:b + 1, :s0 + T].numpy(),
+                              pos[b:b + 1, :s0 + T].numpy(), L.kind, L.window, L.theta,
+                              L.rot_dim, H, Hkv, rows=rows)
+        check_close(out[b], want, f"chunk b={b} start={s0} kind={kind} T={T} cap={cap}")
+    # decode of the next token continues each sequence
+    nq = torch.stack([qkv[b, s0 + T] for b, s0 in enumerate(starts)]).contiguous()
+    ng = torch.stack([gate[b, s0 + T] for b, s0 in enumerate(starts)]).contiguous()
+    npos = torch.tensor([s0 + T for s0 in starts], dtype=torch.int32)
+    dout = fga.spark_attn_decode(nq.to(cuda), ng.to(cuda), npos.to(cuda), kc, vc, layer)
+    for b, s0 in enumerate(starts):
+        want = oracle.prefill(qb[b:b + 1, :s0 + T + 1], gate[b:b + 1, :s0 + T + 1].numpy(),
+                              pos[b:b + 1, :s0 + T + 1].numpy(), L.kind, L.window, L.theta,
+                              L.rot_dim, H, Hkv, rows=np.array([s0 + T], np.int64))
+        check_close(dout[b:b + 1], want, f"decode after chunk b={b} kind={kind}")
+
+
+def test_chunked_prefill_ring_rules(cuda):
+    layer = wl.SLIDING_LAYER
+    q = torch.zeros((1, 64, 24 * 256), dtype=torch.bfloat16, device=cuda)
+    g = torch.zeros((1, 64, 16), device=cuda)
+    p = torch.zeros((1, 64), dtype=torch.int32, device=cuda)
+    st = torch.zeros((1,), dtype=torch.int32, device=cuda)
+    for cap, code in ((512, 5), (600, 3)):   # too small for the chunk; not a multiple of 128
+        kc = torch.zeros((1, 4, cap, 256), dtype=torch.bfloat16, device=cuda)
+        with pytest.raises(fga.SparkError) as e:
+            fga.spark_attn_prefill_chunk(q, g, p, kc, kc.clone(), st, layer)
+        assert e.value.status == code
