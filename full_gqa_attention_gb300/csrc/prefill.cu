@@ -655,7 +655,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int c = 0; c < 4; ++c)
                     tma_store_4d(&tm_out, qbuf + c * kSlotBytes, c * 64, g * G, t0, b);
                 tma_store_commit();
-                tma_store_wait_all();
+                tma_store_wait_read();  // the staging buffer is read; the writes land by grid end
             }
         }
         tc_fence_before();

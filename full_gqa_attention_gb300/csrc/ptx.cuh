@@ -149,6 +149,12 @@ __device__ __forceinline__ void tma_store_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Waits until every committed bulk store has finished reading shared memory
+// (their global writes may still be in flight).
+__device__ __forceinline__ void tma_store_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // Makes this thread's generic-proxy shared-memory writes visible to the async
 // proxy (TMA, tensor cores).
 __device__ __forceinline__ void fence_proxy_async_smem() {

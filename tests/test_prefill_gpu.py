@@ -68,6 +68,18 @@ def test_sliding_layer_lengths(cuda, T):
                              seed=100 + T))
 
 
+# Grids of one to several waves of CTAs over 152 SMs, with query tiles of 1
+# to 10 key tiles and every group size the kernel packs (G = 1, 4): each CTA
+# must write its whole output tile, whatever runs beside it.
+@pytest.mark.parametrize("kind,B,T,H,Hkv", [(SLIDING, 2, 1300, 16, 4), (FULL, 2, 1300, 16, 4),
+                                            (SLIDING, 4, 1216, 8, 2), (FULL, 3, 1000, 8, 8),
+                                            (SLIDING, 1, 2600, 16, 4), (FULL, 2, 2432, 8, 2)])
+def test_item_lists_per_cta(cuda, kind, B, T, H, Hkv):
+    layer = wl.FULL_LAYER if kind == FULL else wl.SLIDING_LAYER
+    case = wl.PrefillCase("items", B=B, T=T, H=H, Hkv=Hkv, layer=layer, seed=7 * T + B)
+    run(cuda, case)
+
+
 @pytest.mark.parametrize("W", [1, 2, 63, 511, 513, 600, 4096])
 def test_windows(cuda, W):
     layer = wl.Layer(kind=SLIDING, window=W, theta=1e4, rot_dim=256)
