@@ -422,9 +422,68 @@ def run_ours(args, rank, world, local):
         "clocks": clocks.summary(),
         "device_status": status,
     }
+    if pre is not None and rank == 0:
+        line["small_prefill"] = time_small_prefill(fga, dev, bf16_peak)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args)
     return line
+
+
+def time_small_prefill(fga, dev, bf16_peak, calls=50):
+    """The 1.7B sliding_attention prefill (B=1, T=1024): 64 query tiles, far
+    fewer than the SMs, so launch latency is a large part of a call.  Timed
+    per call back to back, and as `calls` calls captured in one CUDA graph.
+    Its 6 MB of inputs stay in L2 between calls."""
+    import torch
+    c = wl.PREFILL_SLIDING_1P7B_T1024
+    x = wl.make_prefill_inputs(c)
+    q, g, p = (x[k].to(dev) for k in ("qkv", "gate", "pos"))
+    out = torch.empty((c.B, c.T, c.H * 256), dtype=torch.bfloat16, device=dev)
+    ws = fga.new_workspace(fga.spark_attn_prefill_workspace_size(c.B, c.T, c.H, c.Hkv, c.layer),
+                           dev)
+
+    def call(stream):
+        fga.spark_attn_prefill(q, g, p, c.layer, out=out, workspace=ws, stream=stream)
+
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(5):
+            call(side)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(side)
+        for _ in range(calls):
+            call(side)
+        s1.record(side)
+    torch.cuda.synchronize()
+    eager_ms = s0.elapsed_time(s1) / calls
+
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(calls):
+            call(torch.cuda.current_stream())
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    graph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = g0.elapsed_time(g1) / calls
+    status = fga.spark_attn_read_status(ws)
+    flops = prefill_flops(c)
+    return {
+        "workload": "prefill 1.7B sliding_attention B=1 T=1024 H=8 Hkv=2 W=512",
+        "flops": flops, "calls": calls, "l2": "resident (6 MB of inputs)",
+        "eager_us_per_call": 1000.0 * eager_ms,
+        "graph_us_per_call": 1000.0 * graph_ms,
+        "tflops_eager": flops / eager_ms / 1e9,
+        "tflops_graph": flops / graph_ms / 1e9,
+        "frac_bf16_peak_graph": flops / graph_ms / 1e9 / bf16_peak,
+        "device_status": status,
+    }
 
 
 # Per-launch DRAM traffic (read + write bytes) from ncu captures of the

@@ -13,8 +13,10 @@ from ._binding import (  # noqa: F401
     SPARK_LAYER_SLIDING,
     SPARK_NOALLOC_SCRATCH_BYTES,
     SPARK_OK,
+    SparkDeviceFault,
     SparkError,
     as_desc,
+    check_device_status,
     layer_desc,
     lib,
     new_workspace,

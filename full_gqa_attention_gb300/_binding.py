@@ -86,6 +86,34 @@ class SparkError(RuntimeError):
         super().__init__(f"{where}: status {status} ({spark_status_str(status)})")
 
 
+class SparkDeviceFault(RuntimeError):
+    """The kernels of a call recorded a device fault (SPARK_DEVERR_* bits)."""
+
+    def __init__(self, bits: int, where: str):
+        self.bits = bits
+        super().__init__(f"{where}: device status 0x{bits:x}")
+
+
+_check_own_workspace = False
+
+
+def check_device_status(enabled: bool = True) -> None:
+    """When enabled, a call that allocates its own workspace (workspace=None)
+    reads that workspace's status word afterwards and raises SparkDeviceFault
+    if it is not zero.  The read synchronizes the stream, so this is off by
+    default; a caller that passes its own workspace reads it itself with
+    spark_attn_read_status."""
+    global _check_own_workspace
+    _check_own_workspace = bool(enabled)
+
+
+def _check_owned(workspace: torch.Tensor, where: str, stream) -> None:
+    if _check_own_workspace:
+        bits = spark_attn_read_status(workspace, stream=stream)
+        if bits:
+            raise SparkDeviceFault(bits, where)
+
+
 def spark_status_str(status: int) -> str:
     return lib.spark_status_str(status).decode()
 
@@ -157,13 +185,16 @@ def spark_attn_prefill(qkv: torch.Tensor, gate: torch.Tensor, pos: torch.Tensor,
         out = torch.empty((B, T, H * HEAD_DIM), dtype=torch.bfloat16, device=qkv.device)
     _need(out, torch.bfloat16, "out")
     need = lib.spark_attn_prefill_workspace_size(B, T, H, Hkv, ctypes.byref(d))
-    if workspace is None:
+    owned = workspace is None
+    if owned:
         workspace = new_workspace(need, qkv.device)
     st = lib.spark_attn_prefill(_ptr(qkv), _ptr(gate), _ptr(pos), ctypes.byref(d), B, T, H,
                                 Hkv, _ptr(out), _ptr(workspace), workspace.numel(),
                                 _stream(stream))
     if st != SPARK_OK:
         raise SparkError(st, "spark_attn_prefill")
+    if owned:
+        _check_owned(workspace, "spark_attn_prefill", stream)
     return out
 
 
@@ -190,7 +221,8 @@ def spark_attn_prefill_cache(qkv: torch.Tensor, gate: torch.Tensor, pos: torch.T
         out = torch.empty((B, T, H * HEAD_DIM), dtype=torch.bfloat16, device=qkv.device)
     _need(out, torch.bfloat16, "out")
     need = lib.spark_attn_prefill_workspace_size(B, T, H, Hkv, ctypes.byref(d))
-    if workspace is None:
+    owned = workspace is None
+    if owned:
         workspace = new_workspace(need, qkv.device)
     st = lib.spark_attn_prefill_cache(_ptr(qkv), _ptr(gate), _ptr(pos), _ptr(k_cache),
                                       _ptr(v_cache), k_cache.shape[2], ctypes.byref(d), B, T, H,
@@ -198,6 +230,8 @@ def spark_attn_prefill_cache(qkv: torch.Tensor, gate: torch.Tensor, pos: torch.T
                                       _stream(stream))
     if st != SPARK_OK:
         raise SparkError(st, "spark_attn_prefill_cache")
+    if owned:
+        _check_owned(workspace, "spark_attn_prefill_cache", stream)
     return out
 
 
@@ -225,7 +259,8 @@ def spark_attn_prefill_chunk(qkv: torch.Tensor, gate: torch.Tensor, pos: torch.T
         out = torch.empty((B, T, H * HEAD_DIM), dtype=torch.bfloat16, device=qkv.device)
     _need(out, torch.bfloat16, "out")
     need = lib.spark_attn_prefill_workspace_size(B, T, H, Hkv, ctypes.byref(d))
-    if workspace is None:
+    owned = workspace is None
+    if owned:
         workspace = new_workspace(need, qkv.device)
     st = lib.spark_attn_prefill_chunk(_ptr(qkv), _ptr(gate), _ptr(pos), _ptr(k_cache),
                                       _ptr(v_cache), k_cache.shape[2], _ptr(start),
@@ -233,6 +268,8 @@ def spark_attn_prefill_chunk(qkv: torch.Tensor, gate: torch.Tensor, pos: torch.T
                                       workspace.numel(), _stream(stream))
     if st != SPARK_OK:
         raise SparkError(st, "spark_attn_prefill_chunk")
+    if owned:
+        _check_owned(workspace, "spark_attn_prefill_chunk", stream)
     return out
 
 
@@ -259,13 +296,16 @@ def spark_attn_decode(qkv: torch.Tensor, gate: torch.Tensor, pos: torch.Tensor,
         out = torch.empty((B, H * HEAD_DIM), dtype=torch.bfloat16, device=qkv.device)
     _need(out, torch.bfloat16, "out")
     need = lib.spark_attn_decode_workspace_size(B, H, Hkv, cap, ctypes.byref(d))
-    if workspace is None:
+    owned = workspace is None
+    if owned:
         workspace = new_workspace(need, qkv.device)
     st = lib.spark_attn_decode(_ptr(qkv), _ptr(gate), _ptr(pos), _ptr(k_cache), _ptr(v_cache),
                                cap, ctypes.byref(d), B, H, Hkv, _ptr(out), _ptr(workspace),
                                workspace.numel(), _stream(stream))
     if st != SPARK_OK:
         raise SparkError(st, "spark_attn_decode")
+    if owned:
+        _check_owned(workspace, "spark_attn_decode", stream)
     return out
 
 

@@ -34,4 +34,7 @@ def cuda():
     if not torch.cuda.is_available():
         pytest.fail("GPU test run without a CUDA device")
     torch.cuda.set_device(0)
+    # calls that allocate their own workspace report device faults too
+    import full_gqa_attention_gb300 as fga
+    fga.check_device_status(True)
     return torch.device("cuda:0")

@@ -170,6 +170,22 @@ def test_bad_position_is_flagged(cuda):
     assert fga.spark_attn_read_status(ws) == 0
 
 
+def test_fault_in_an_owned_workspace_is_raised(cuda):
+    """With check_device_status on (the GPU test session turns it on), a call
+    that allocates its own workspace raises the device fault it recorded."""
+    layer = wl.FULL_LAYER
+    B, H, Hkv, cap = 1, 16, 4, 128
+    case = wl.DecodeCase("t", B=B, H=H, Hkv=Hkv, layer=layer, seed=11, cap=cap, len_lo=0,
+                         len_hi=0)
+    step = wl.make_decode_step_inputs(case)
+    kc = torch.zeros((B, Hkv, cap, 256), dtype=torch.bfloat16, device=cuda)
+    vc = torch.zeros_like(kc)
+    pos = torch.tensor([cap], dtype=torch.int32, device=cuda)
+    with pytest.raises(fga.SparkDeviceFault) as err:
+        fga.spark_attn_decode(step["qkv"].to(cuda), step["gate"].to(cuda), pos, kc, vc, layer)
+    assert err.value.bits == fga.SPARK_DEVERR_POSITION
+
+
 def _full_size(cuda, dcase, sample_b):
     """Full-size decode; the oracle checks the sampled sequences."""
     step = wl.make_decode_step_inputs(dcase)
