@@ -8,14 +8,13 @@
 #include <cstdint>
 #include <utility>
 
+#include "bands.cuh"
 #include "ptx.cuh"
 
 namespace spark {
 
 constexpr int kHeadDim = 256;
 constexpr int kMaxRopePairs = kHeadDim / 2;
-constexpr int kLayerFull = 0;
-constexpr int kLayerSliding = 1;
 
 // log2(e) / sqrt(256): scores are kept in base-2 units, s * kScaleLog2.
 constexpr float kScaleLog2 = 1.4426950408889634f / 16.0f;

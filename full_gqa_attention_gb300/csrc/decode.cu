@@ -33,15 +33,6 @@ constexpr int kDecQBytes = 8 * kHeadDim * 2;              // 8 (padded) query he
 constexpr int kDecSmemBytes = 1024 + kDecStages * kDecStageBytes + kDecQBytes +
                               2 * kDecStages * 8;
 
-// Slot s (s < min(pos, cap)) of a ring of `cap` slots holds the latest token
-// j < pos with j = s (mod cap).  It is visible from the new token at `pos`
-// iff pos - j < window.
-__device__ __forceinline__ bool ring_slot_visible(long long s, long long pos, long long cap,
-                                                  int window) {
-    const long long j = s + cap * ((pos - 1 - s) / cap);
-    return pos - j < (long long)window;
-}
-
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -71,7 +62,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         return;
     }
     // Scanned slots: full layer -> tokens [0, pos); ring -> slots [0, min(pos, cap)).
-    const long long n_scan = (P.kind == kLayerFull) ? p : (p < P.cap ? p : P.cap);
+    const long long n_scan = decode_scan_slots(P.kind, p, P.cap);
     const long long c_lo = static_cast<long long>(split) * P.chunk;
     const long long c_hi = (c_lo + P.chunk < n_scan) ? c_lo + P.chunk : n_scan;
     if (c_lo >= c_hi) return;  // empty split: the merge does not read it
@@ -398,7 +389,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant
 
     // merge the new token with the partial states of the non-empty splits:
     // the maximum lane-parallel, then the weighted sums, several splits in flight
-    const long long n_scan = (P.kind == kLayerFull) ? p : (p < P.cap ? p : P.cap);
+    const long long n_scan = decode_scan_slots(P.kind, p, P.cap);
     const int nvalid = static_cast<int>((n_scan + P.chunk - 1) / P.chunk);
     const size_t part0 = (static_cast<size_t>(b) * P.H + h) * P.nsplit;
     float M = x_new;

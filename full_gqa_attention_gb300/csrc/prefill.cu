@@ -329,12 +329,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (skip && tid == 0 && qtile == P.n_qtiles - 1 && g == 0) atomicOr(P.status, kErrPosition);
     }
     const int a0 = start + t0;
-    int kv_lo = (P.kind == kLayerFull) ? 0 : (a0 - P.window + 1 > 0 ? a0 - P.window + 1 : 0);
     // a ring is read in 128-key tiles aligned to its 128-slot boundaries, so
     // that no tile wraps around the end of the ring
-    if (kFromCache && P.kind == kLayerSliding) kv_lo &= ~(kBN - 1);
-    const int kv_hi = start + t_end;
-    const int ntiles = skip ? 0 : (kv_hi - kv_lo + kBN - 1) / kBN;
+    const KeyTiles kt = prefill_key_tiles(P.kind, P.window, a0, start + t_end, kBN,
+                                          kFromCache && P.kind == kLayerSliding);
+    const int kv_lo = kt.kv_lo;
+    const int ntiles = skip ? 0 : kt.ntiles;
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -551,14 +551,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
             for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(sv[c]);
             const int key0 = kv_lo + j * kBN;
-            const bool need_mask = (key0 + kBN - 1 > a0) ||
-                                   (P.kind == kLayerSliding && a_last - key0 >= P.window);
-            if (need_mask) {
+            if (tile_needs_mask(P.kind, P.window, key0, kBN, a0, a_last)) {
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
-                    const int key = key0 + col0 + c;
-                    const bool vis =
-                        key <= tok_abs && (P.kind == kLayerFull || tok_abs - key < P.window);
+                    const bool vis = key_visible(P.kind, P.window, tok_abs, key0 + col0 + c);
                     x[c] = vis ? x[c] : -INFINITY;
                 }
             }
