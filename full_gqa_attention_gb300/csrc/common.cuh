@@ -10,6 +10,7 @@
 
 #include "bands.cuh"
 #include "ptx.cuh"
+#include "rope_math.cuh"
 
 namespace spark {
 
@@ -30,24 +31,10 @@ struct RopeTable {
     int rot_dim;
 };
 
-// cos and sin of the RoPE angle of one pair at an integer position.
-//
-// The angle pos * inv_freq reaches 1e6 rad at the 1M-token positions of the
-// full layers, where a plain fp32 product is off by up to ~0.03 rad.  Instead
-// the angle is taken in turns and reduced exactly: with fp = pos (exact below
-// 2^24) and u = u_hi + u_lo,
-//   p = fl(fp * u_hi),  e = fp * u_hi - p  (exact, by fma),
-//   p - rint(p)         (exact: p and its nearest integer share the exponent),
-//   t = (p - rint(p)) + (fp * u_lo + e)   in [-1/2, 1/2] up to rounding,
-// so only the last two roundings (~2^-25 turns, ~2e-7 rad) remain before
-// sincospif.  Explicit _rn intrinsics keep the compiler from fusing the
-// products into neighbouring adds, which would count e twice.
+// cos and sin of the RoPE angle of one pair at an integer position: the
+// exact reduction in turns of rope_math.cuh, then sincospif.
 __device__ __forceinline__ void rope_cos_sin(int pos, float2 u, float &c, float &s) {
-    const float fp = static_cast<float>(pos);
-    const float p = __fmul_rn(fp, u.x);
-    const float e = __fmaf_rn(fp, u.x, -p);
-    const float f = __fsub_rn(p, rintf(p));
-    const float t = __fadd_rn(f, __fmaf_rn(fp, u.y, e));
+    const float t = rope_turns(pos, u.x, u.y);
     sincospif(__fmul_rn(2.0f, t), &s, &c);
 }
 
@@ -124,6 +111,8 @@ struct PrefillParams {
     int gate_mode;             // 0 sigmoid, 1 silu
     int rot_w;                 // rot_dim rounded up to 64: leading K dims read from krot
     int n_qtiles;              // query tiles per (b, kv head)
+    int wave;                  // CTAs resident at once (one per SM): a CTA pulls the
+                               // query tile of CTA blockIdx + wave into L2
     RopeTable rope;
 };
 

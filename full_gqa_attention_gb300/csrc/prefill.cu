@@ -344,6 +344,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
             for (int c = 0; c < 4; ++c)
                 tma_load_4d(qbuf + c * kSlotBytes, &tm_q, &bars[kBarQFull], c * 64, g * G, t0, b);
+            // the CTA one wave later (likely the next one on this SM) finds its
+            // query tile in L2
+            const long long nb = static_cast<long long>(blockIdx.x) + P.wave;
+            if (P.wave > 0 && nb < gridDim.x) {
+                const int nq = P.n_qtiles - 1 - static_cast<int>(nb / units);
+                const int nrem = static_cast<int>(nb % units);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    tma_prefetch_l2_4d(&tm_q, c * 64, (nrem % P.Hkv) * G, nq * tq, nrem / P.Hkv);
+            }
             bool ok = true;
             auto next_slot = [&](int &slot) -> bool {
                 slot = sc % kSlots;

@@ -281,6 +281,7 @@ spark_status prefill_impl(const void *qkv, const float *gate, const int32_t *pos
     P.gate_mode = desc->gate_mode;
     P.rot_w = pl.rot_w;
     P.n_qtiles = (T + tq - 1) / tq;
+    P.wave = sm_count_or_default();
     make_rope_table(desc, &P.rope);
 
     const uint64_t heads = static_cast<uint64_t>(H + 2 * Hkv);
