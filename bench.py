@@ -490,10 +490,10 @@ def time_small_prefill(fga, dev, bf16_peak, calls=50):
 # current kernels, scaled to one launch of the bench workload; None when the
 # kernels changed since the counters were taken.
 # decode_split_kernel: 540.0 MB in a 131,072-token capture, scaled x8 to the
-# 1,048,576-token layer; prefill_attn_kernel: 492.8 MB measured on this workload.
+# 1,048,576-token layer; prefill_attn_kernel: 491.2 MB measured on this workload.
 TRAFFIC: dict[str, float | None] = {
     "decode_split_kernel": 539.981056e6 * 8,
-    "prefill_attn_kernel": 492.764672e6,
+    "prefill_attn_kernel": 491.213568e6,
 }
 
 

@@ -188,6 +188,7 @@ constexpr int kSlotBytes = 16384;         // ring slot: 128 keys x 64 dims (K) o
 constexpr int kSlots = 8;
 constexpr int kQBytes = 4 * kSlotBytes;   // 128 rows x 256 dims, as 4 chunks of 64 dims
 constexpr int kAttnThreads = 384;
+constexpr int kPrefetchMaxTiles = 8;      // CTAs this short pull the next wave's Q into L2
 constexpr int kSoftmaxWarp0 = 4;
 constexpr int kSoftmaxThreads = 256;        // two warpgroups, 64 score columns each
 constexpr uint32_t kTmemCols = 512;
@@ -345,9 +346,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int c = 0; c < 4; ++c)
                 tma_load_4d(qbuf + c * kSlotBytes, &tm_q, &bars[kBarQFull], c * 64, g * G, t0, b);
             // the CTA one wave later (likely the next one on this SM) finds its
-            // query tile in L2
+            // query tile in L2 -- when this CTA is short (a sliding layer's, or
+            // the last waves of a causal one); behind a long CTA the tile would
+            // be evicted before use and read twice
             const long long nb = static_cast<long long>(blockIdx.x) + P.wave;
-            if (P.wave > 0 && nb < gridDim.x) {
+            if (P.wave > 0 && nb < gridDim.x && ntiles <= kPrefetchMaxTiles) {
                 const int nq = P.n_qtiles - 1 - static_cast<int>(nb / units);
                 const int nrem = static_cast<int>(nb % units);
 #pragma unroll
