@@ -174,3 +174,68 @@ def prefill(*args, **kw):
 
 def decode(*args, **kw):
     return default().decode(*args, **kw)
+
+
+# ---------------------------------------------------------------- whole layer
+#
+# Spark-X2.5 architecture (4B / 1.7B), §3 Eq. 1 and Fig. 1: the attention
+# block takes the normed hidden state x; q_k_v_proj (hidden -> (H+2Hkv)*256)
+# and g_proj (hidden -> H, one gate logit per head) feed the core, and
+# out_proj (H*256 -> hidden) maps the gated attention output back.  §1: the
+# released checkpoints run in bfloat16, and §3: the gated output is cast back
+# to the weight dtype.  Reading taken: every Linear's output is a bf16 tensor
+# (rounded to nearest even from the exact product); the block output y is
+# returned unrounded, in fp64.  No biases (the pages list none).
+
+
+def bf16_round_bits(v: np.ndarray) -> np.ndarray:
+    """fp64 values -> bf16 bit patterns, round to nearest even, exactly
+    (no intermediate fp32 rounding).  Finite, normal-range inputs only."""
+    v = np.asarray(v, np.float64)
+    m, e = np.frexp(v)                      # v = m * 2^e, 0.5 <= |m| < 1
+    q = np.rint(m * 256.0) / 256.0          # 8 significant bits, ties to even
+    r = np.ldexp(q, e).astype(np.float32)   # exact in fp32
+    return (r.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> fp64 (exact)."""
+    b = np.asarray(bits, np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def layer_prefill(x_bits, w_qkv_bits, w_g_bits, w_o_bits, pos, kind, window, theta,
+                  rot_dim, H, Hkv, rows=None, gate_mode=0):
+    """Oracle of the attention block over a prefill.
+
+    x_bits: uint16 [B, T, hidden]; w_qkv_bits [(H+2Hkv)*256, hidden];
+    w_g_bits [H, hidden]; w_o_bits [hidden, H*256] (bf16 patterns, PyTorch
+    Linear layout: y = x W^T); pos int32 [B, T].  rows: optional flat row ids
+    (b*T + t) of y to compute.  Returns fp64 y [B, T, hidden] or
+    [len(rows), hidden].
+    """
+    x = bits_to_f64(x_bits)
+    B, T, hidden = x.shape
+    qkv_bits = bf16_round_bits(x @ bits_to_f64(w_qkv_bits).T)          # q_k_v_proj
+    g = bits_to_f64(bf16_round_bits(x @ bits_to_f64(w_g_bits).T))      # g_proj
+    a = prefill(qkv_bits, g.astype(np.float32), pos, kind, window, theta, rot_dim, H, Hkv,
+                rows=rows, gate_mode=gate_mode)                        # Eq. 1
+    a = bits_to_f64(bf16_round_bits(a))                                # cast to bf16
+    return a @ bits_to_f64(w_o_bits).T                                 # out_proj
+
+
+def layer_decode(x_bits, w_qkv_bits, w_g_bits, w_o_bits, pos, k_cache_bits, v_cache_bits,
+                 kind, window, theta, rot_dim, H, Hkv, gate_mode=0):
+    """Oracle of the attention block for one decode step.
+
+    x_bits: uint16 [B, hidden]; weights as in layer_prefill; pos int32 [B];
+    caches uint16 [B, Hkv, cap, 256] BEFORE the step.  Returns (y fp64
+    [B, hidden], k_new, v_new) with k_new / v_new as in decode().
+    """
+    x = bits_to_f64(x_bits).reshape(np.asarray(x_bits).shape[0], -1)
+    qkv_bits = bf16_round_bits(x @ bits_to_f64(w_qkv_bits).T)
+    g = bits_to_f64(bf16_round_bits(x @ bits_to_f64(w_g_bits).T))
+    a, k_new, v_new = decode(qkv_bits, g.astype(np.float32), pos, k_cache_bits, v_cache_bits,
+                             kind, window, theta, rot_dim, H, Hkv, gate_mode=gate_mode)
+    a = bits_to_f64(bf16_round_bits(a))
+    return a @ bits_to_f64(w_o_bits).T, k_new, v_new

@@ -233,3 +233,24 @@ def test_empty_batch(cuda):
                                 torch.empty((0, 4, 512, 256), dtype=torch.bfloat16, device=cuda),
                                 layer)
     assert out.shape == (0, 16 * 256)
+
+
+@pytest.mark.parametrize("H,Hkv", [(16, 4), (8, 2), (8, 8)])
+def test_window_one_passes_v_through_bit_exact(cuda, H, Hkv):
+    """Window 1 on a 512-slot ring: every cached slot is outside the window,
+    so the output is the new token's V slice of KV head h // (H/Hkv), times
+    sigmoid(40) = 1 in fp32, bit for bit (layout pin on the decode path)."""
+    G = H // Hkv
+    layer = wl.Layer(kind=SLIDING, window=1, theta=1e4, rot_dim=256)
+    B, cap = 3, 512
+    case = wl.DecodeCase("w1", B=B, H=H, Hkv=Hkv, layer=layer, seed=21, cap=cap, len_lo=0,
+                         len_hi=0)
+    step = wl.make_decode_step_inputs(case)
+    kc = wl.fill_cache_(torch.empty((B, Hkv, cap, 256), dtype=torch.bfloat16), 22).to(cuda)
+    vc = wl.fill_cache_(torch.empty((B, Hkv, cap, 256), dtype=torch.bfloat16), 23).to(cuda)
+    pos = torch.tensor([0, 700, 511], dtype=torch.int32, device=cuda)
+    out = fga.spark_attn_decode(step["qkv"].to(cuda), torch.full((B, H), 40.0, device=cuda),
+                                pos, kc, vc, layer)
+    v = step["qkv"][:, (H + Hkv) * 256:].reshape(B, Hkv, 256)
+    want = v[:, torch.arange(H) // G, :].reshape(B, H * 256)
+    assert torch.equal(out.reshape(B, H * 256).cpu(), want)

@@ -220,3 +220,20 @@ def test_empty(cuda):
                                  torch.empty((1, 0), dtype=torch.int32, device=cuda),
                                  wl.FULL_LAYER)
     assert out.shape == (1, 0, 16 * 256)
+
+
+@pytest.mark.parametrize("H,Hkv,rot", [(16, 4, 256), (8, 2, 64), (8, 8, 0), (8, 1, 128)])
+def test_window_one_passes_v_through_bit_exact(cuda, H, Hkv, rot):
+    """Window 1: each row sees only its own token, so p = 1 and the output is
+    that token's V slice of KV head h // (H/Hkv), times sigmoid(40) = 1 in
+    fp32: bit for bit.  Pins the Q|K|V layout of qkv, the head-to-KV-head map
+    and the output layout (Spark §3, Fig. 1) on the GPU."""
+    G = H // Hkv
+    case = wl.PrefillCase("w1", B=2, T=200, H=H, Hkv=Hkv,
+                          layer=wl.Layer(kind=SLIDING, window=1, theta=1e4, rot_dim=rot), seed=13)
+    x = wl.make_prefill_inputs(case)
+    out = fga.spark_attn_prefill(x["qkv"].to(cuda), torch.full((2, 200, H), 40.0, device=cuda),
+                                 x["pos"].to(cuda), case.layer)
+    v = x["qkv"][:, :, (H + Hkv) * 256:].reshape(2, 200, Hkv, 256)
+    want = v[:, :, torch.arange(H) // G, :].reshape(2, 200, H * 256)
+    assert torch.equal(out.cpu(), want)
