@@ -23,6 +23,10 @@ from ._binding import (  # noqa: F401
     spark_attn_decode,
     spark_attn_decode_noalloc,
     spark_attn_decode_workspace_size,
+    spark_attn_layer_decode,
+    spark_attn_layer_decode_workspace_size,
+    spark_attn_layer_prefill,
+    spark_attn_layer_prefill_workspace_size,
     spark_attn_prefill,
     spark_attn_prefill_cache,
     spark_attn_prefill_chunk,

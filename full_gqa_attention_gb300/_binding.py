@@ -68,6 +68,16 @@ def _load() -> ctypes.CDLL:
     lib.spark_attn_decode.restype = i32
     lib.spark_attn_decode_noalloc.argtypes = [P, P, P, P, P, i64, D, i32, i32, i32, P, P, P]
     lib.spark_attn_decode_noalloc.restype = i32
+    lib.spark_attn_layer_prefill_workspace_size.argtypes = [i32, i32, i32, i32, i32, D]
+    lib.spark_attn_layer_prefill_workspace_size.restype = sz
+    lib.spark_attn_layer_prefill.argtypes = [P, P, P, P, P, P, P, i64, D, i32, i32, i32, i32,
+                                             i32, P, P, sz, P]
+    lib.spark_attn_layer_prefill.restype = i32
+    lib.spark_attn_layer_decode_workspace_size.argtypes = [i32, i32, i32, i32, i64, D]
+    lib.spark_attn_layer_decode_workspace_size.restype = sz
+    lib.spark_attn_layer_decode.argtypes = [P, P, P, P, P, P, P, i64, D, i32, i32, i32, i32, P,
+                                            P, sz, P]
+    lib.spark_attn_layer_decode.restype = i32
     lib.spark_attn_read_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), i32, P]
     lib.spark_attn_read_status.restype = i32
     lib.spark_status_str.argtypes = [i32]
@@ -342,6 +352,108 @@ def spark_attn_decode_noalloc(qkv: torch.Tensor, gate: torch.Tensor, pos: torch.
     if st != SPARK_OK:
         raise SparkError(st, "spark_attn_decode_noalloc")
     return out
+
+
+def _layer_weights(w_qkv, w_g, w_o, hidden: int):
+    for t, name in ((w_qkv, "w_qkv"), (w_g, "w_g"), (w_o, "w_o")):
+        _need(t, torch.bfloat16, name)
+    H = w_g.shape[0]
+    Hkv = (w_qkv.shape[0] // HEAD_DIM - H) // 2
+    if (w_g.shape != (H, hidden) or w_qkv.shape != ((H + 2 * Hkv) * HEAD_DIM, hidden)
+            or w_o.shape != (hidden, H * HEAD_DIM)):
+        raise ValueError("inconsistent projection weight shapes")
+    return H, Hkv
+
+
+def spark_attn_layer_prefill_workspace_size(B: int, T: int, hidden: int, H: int, Hkv: int,
+                                            layer) -> int:
+    d = as_desc(layer)
+    return lib.spark_attn_layer_prefill_workspace_size(B, T, hidden, H, Hkv, ctypes.byref(d))
+
+
+def spark_attn_layer_decode_workspace_size(B: int, hidden: int, H: int, Hkv: int, cap: int,
+                                           layer) -> int:
+    d = as_desc(layer)
+    return lib.spark_attn_layer_decode_workspace_size(B, hidden, H, Hkv, cap, ctypes.byref(d))
+
+
+def spark_attn_layer_prefill(x: torch.Tensor, w_qkv: torch.Tensor, w_g: torch.Tensor,
+                             w_o: torch.Tensor, pos: torch.Tensor, layer,
+                             k_cache: torch.Tensor | None = None,
+                             v_cache: torch.Tensor | None = None,
+                             y: torch.Tensor | None = None,
+                             workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The attention block over a prefill: x bf16 [B,T,hidden] (normed hidden
+    state), Linear weights w_qkv [(H+2Hkv)*256, hidden], w_g [H, hidden],
+    w_o [hidden, H*256], pos int32 [B,T] -> y bf16 [B,T,hidden].  With caches
+    (bf16 [B,Hkv,cap,256]) it also fills the decode cache."""
+    _need(x, torch.bfloat16, "x")
+    _need(pos, torch.int32, "pos")
+    B, T, hidden = x.shape
+    H, Hkv = _layer_weights(w_qkv, w_g, w_o, hidden)
+    if pos.shape != (B, T):
+        raise ValueError("inconsistent layer prefill shapes")
+    cap = 0
+    if k_cache is not None or v_cache is not None:
+        _need(k_cache, torch.bfloat16, "k_cache")
+        _need(v_cache, torch.bfloat16, "v_cache")
+        if (k_cache.shape != v_cache.shape or k_cache.shape[:2] != (B, Hkv)
+                or k_cache.shape[3] != HEAD_DIM):
+            raise ValueError("inconsistent cache shapes")
+        cap = k_cache.shape[2]
+    d = as_desc(layer)
+    if y is None:
+        y = torch.empty((B, T, hidden), dtype=torch.bfloat16, device=x.device)
+    _need(y, torch.bfloat16, "y")
+    need = lib.spark_attn_layer_prefill_workspace_size(B, T, hidden, H, Hkv, ctypes.byref(d))
+    owned = workspace is None
+    if owned:
+        workspace = new_workspace(need, x.device)
+    st = lib.spark_attn_layer_prefill(_ptr(x), _ptr(w_qkv), _ptr(w_g), _ptr(w_o), _ptr(pos),
+                                      _ptr(k_cache), _ptr(v_cache), cap, ctypes.byref(d), B, T,
+                                      hidden, H, Hkv, _ptr(y), _ptr(workspace), workspace.numel(),
+                                      _stream(stream))
+    if st != SPARK_OK:
+        raise SparkError(st, "spark_attn_layer_prefill")
+    if owned:
+        _check_owned(workspace, "spark_attn_layer_prefill", stream)
+    return y
+
+
+def spark_attn_layer_decode(x: torch.Tensor, w_qkv: torch.Tensor, w_g: torch.Tensor,
+                            w_o: torch.Tensor, pos: torch.Tensor, k_cache: torch.Tensor,
+                            v_cache: torch.Tensor, layer, y: torch.Tensor | None = None,
+                            workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The attention block for one decode step: x bf16 [B,hidden], weights as
+    for spark_attn_layer_prefill, pos int32 [B], caches bf16 [B,Hkv,cap,256]
+    (updated in place) -> y bf16 [B,hidden]."""
+    _need(x, torch.bfloat16, "x")
+    _need(pos, torch.int32, "pos")
+    _need(k_cache, torch.bfloat16, "k_cache")
+    _need(v_cache, torch.bfloat16, "v_cache")
+    B, hidden = x.shape
+    H, Hkv = _layer_weights(w_qkv, w_g, w_o, hidden)
+    if (pos.shape != (B,) or k_cache.shape != v_cache.shape or k_cache.shape[:2] != (B, Hkv)
+            or k_cache.shape[3] != HEAD_DIM):
+        raise ValueError("inconsistent layer decode shapes")
+    cap = k_cache.shape[2]
+    d = as_desc(layer)
+    if y is None:
+        y = torch.empty((B, hidden), dtype=torch.bfloat16, device=x.device)
+    _need(y, torch.bfloat16, "y")
+    need = lib.spark_attn_layer_decode_workspace_size(B, hidden, H, Hkv, cap, ctypes.byref(d))
+    owned = workspace is None
+    if owned:
+        workspace = new_workspace(need, x.device)
+    st = lib.spark_attn_layer_decode(_ptr(x), _ptr(w_qkv), _ptr(w_g), _ptr(w_o), _ptr(pos),
+                                     _ptr(k_cache), _ptr(v_cache), cap, ctypes.byref(d), B, hidden,
+                                     H, Hkv, _ptr(y), _ptr(workspace), workspace.numel(),
+                                     _stream(stream))
+    if st != SPARK_OK:
+        raise SparkError(st, "spark_attn_layer_decode")
+    if owned:
+        _check_owned(workspace, "spark_attn_layer_decode", stream)
+    return y
 
 
 def spark_attn_read_status(workspace: torch.Tensor, clear: bool = False, stream=None) -> int:

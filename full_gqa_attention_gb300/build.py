@@ -23,8 +23,16 @@ NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
               "-I" + INCLUDE, "-I" + CSRC]
 
 
+def _cuda_home() -> str:
+    return os.environ.get("CUDA_HOME", "/usr/local/cuda")
+
+
+# the layer calls run their projections through cuBLASLt
+LINK_FLAGS = ["-lcublasLt", "-Xlinker", "-rpath=" + os.path.join(_cuda_home(), "lib64")]
+
+
 def _nvcc() -> str:
-    cand = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
+    cand = os.path.join(_cuda_home(), "bin", "nvcc")
     return cand if os.path.exists(cand) else "nvcc"
 
 
@@ -62,7 +70,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with cf.ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, sources()))
     tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
+    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, *LINK_FLAGS]
     if verbose:
         print(" ".join(cmd), flush=True)
     subprocess.run(cmd, check=True)

@@ -1,0 +1,260 @@
+// layer.cu -- the attention block around the core: q_k_v_proj and g_proj on
+// the normed hidden state, the core (prefill or one decode step), out_proj.
+//
+// Spark-X2.5 architecture (4B / 1.7B), §3 Eq. 1 and Fig. 1: a fused
+// q_k_v_proj (hidden -> (H + 2 Hkv) * 256) and a separate g_proj (hidden -> H,
+// one gate logit per head) read the normed hidden state; out_proj
+// (H * 256 -> hidden) maps the gated attention output back.  §1: the
+// checkpoints run in bfloat16 and the pages list no biases.
+//
+// The three projections are plain dense GEMMs and run through cuBLASLt (bf16
+// operands, fp32 accumulation) on the caller's stream, with the caller's
+// workspace as cuBLASLt's scratch.  The gate GEMM accumulates in fp32 and a
+// small kernel rounds its result to bf16, the dtype of the Linear's output,
+// before the core's epilogue takes sigmoid of it in fp32.
+#include <cublasLt.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "spark_attn.h"
+
+namespace spark {
+
+spark_status prefill_impl(const void *qkv, const float *gate, const int32_t *pos,
+                          const spark_layer_desc *desc, int B, int T, int H, int Hkv, void *out,
+                          void *k_cache, void *v_cache, int64_t cap, const int32_t *start,
+                          void *workspace, size_t workspace_bytes, void *stream,
+                          bool validate_only);
+spark_status decode_impl(const void *qkv, const float *gate, const int32_t *pos, void *k_cache,
+                         void *v_cache, int64_t cap, const spark_layer_desc *desc, int B, int H,
+                         int Hkv, void *out, void *workspace, size_t workspace_bytes,
+                         void *stream, bool validate_only);
+
+namespace {
+
+constexpr size_t kLtWorkspace = 32u << 20;  // cuBLASLt scratch inside the caller's workspace
+constexpr int kMaxDevices = 64;
+
+// Rounds fp32 gate logits to bf16 precision in place (round to nearest even).
+__global__ void round_gate_kernel(float *g, long long n) {
+    grid_dep_wait();
+    grid_dep_launch();
+    const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i < n) g[i] = __bfloat162float(__float2bfloat16_rn(g[i]));
+}
+
+std::mutex g_lt_mu;
+cublasLtHandle_t g_lt[kMaxDevices] = {};
+
+// One cuBLASLt handle per device, created on first use.
+cublasLtHandle_t lt_handle() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_lt_mu);
+    if (!g_lt[dev] && cublasLtCreate(&g_lt[dev]) != CUBLAS_STATUS_SUCCESS) g_lt[dev] = nullptr;
+    return g_lt[dev];
+}
+
+// y[M, N] = x[M, K] * W[N, K]^T: row-major bf16 x and W (a PyTorch Linear
+// weight), y bf16 or fp32 row-major, fp32 accumulation.  In cuBLAS's
+// column-major terms: y^T (N x M) = W (stored K x N, transposed) * x^T (K x M).
+bool linear(cublasLtHandle_t h, const void *x, const void *w, void *y, cudaDataType_t y_type,
+            int M, int N, int K, void *lt_ws, cudaStream_t stream) {
+    cublasLtMatmulDesc_t op = nullptr;
+    cublasLtMatrixLayout_t la = nullptr, lb = nullptr, lc = nullptr;
+    cublasLtMatmulPreference_t pref = nullptr;
+    bool ok = false;
+    do {
+        if (cublasLtMatmulDescCreate(&op, CUBLAS_COMPUTE_32F, CUDA_R_32F) != CUBLAS_STATUS_SUCCESS)
+            break;
+        const cublasOperation_t ta = CUBLAS_OP_T, tb = CUBLAS_OP_N;
+        if (cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSA, &ta, sizeof(ta)) !=
+                CUBLAS_STATUS_SUCCESS ||
+            cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSB, &tb, sizeof(tb)) !=
+                CUBLAS_STATUS_SUCCESS)
+            break;
+        if (cublasLtMatrixLayoutCreate(&la, CUDA_R_16BF, K, N, K) != CUBLAS_STATUS_SUCCESS ||
+            cublasLtMatrixLayoutCreate(&lb, CUDA_R_16BF, K, M, K) != CUBLAS_STATUS_SUCCESS ||
+            cublasLtMatrixLayoutCreate(&lc, y_type, N, M, N) != CUBLAS_STATUS_SUCCESS)
+            break;
+        if (cublasLtMatmulPreferenceCreate(&pref) != CUBLAS_STATUS_SUCCESS) break;
+        const size_t ws_bytes = kLtWorkspace;
+        if (cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES,
+                                                 &ws_bytes, sizeof(ws_bytes)) !=
+            CUBLAS_STATUS_SUCCESS)
+            break;
+        cublasLtMatmulHeuristicResult_t res;
+        int found = 0;
+        if (cublasLtMatmulAlgoGetHeuristic(h, op, la, lb, lc, lc, pref, 1, &res, &found) !=
+                CUBLAS_STATUS_SUCCESS ||
+            found < 1)
+            break;
+        const float alpha = 1.0f, beta = 0.0f;
+        ok = cublasLtMatmul(h, op, &alpha, w, la, x, lb, &beta, y, lc, y, lc, &res.algo, lt_ws,
+                            ws_bytes, stream) == CUBLAS_STATUS_SUCCESS;
+    } while (false);
+    if (pref) cublasLtMatmulPreferenceDestroy(pref);
+    if (lc) cublasLtMatrixLayoutDestroy(lc);
+    if (lb) cublasLtMatrixLayoutDestroy(lb);
+    if (la) cublasLtMatrixLayoutDestroy(la);
+    if (op) cublasLtMatmulDescDestroy(op);
+    return ok;
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// The layer workspace: the core's workspace first (its status word is the
+// layer's), then qkv, gate logits, the gated attention output and the
+// cuBLASLt scratch.
+struct LayerPlan {
+    size_t core, qkv, gate, attn, lt, bytes;
+};
+
+LayerPlan plan_layer(size_t core_bytes, long long rows, int H, int Hkv) {
+    LayerPlan pl{};
+    pl.core = 0;
+    pl.qkv = align256(core_bytes);
+    pl.gate = pl.qkv + align256(static_cast<size_t>(rows) * (H + 2 * Hkv) * kHeadDim * 2);
+    pl.attn = pl.gate + align256(static_cast<size_t>(rows) * H * 4);
+    pl.lt = pl.attn + align256(static_cast<size_t>(rows) * H * kHeadDim * 2);
+    pl.bytes = pl.lt + kLtWorkspace;
+    return pl;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+spark_status check_hidden(int hidden) {
+    if (hidden <= 0) return SPARK_ERR_SHAPE;
+    if (hidden % 8 != 0) return SPARK_ERR_UNSUPPORTED;  // rows of 16 bytes
+    return SPARK_OK;
+}
+
+// q_k_v_proj and g_proj of `rows` hidden states into the workspace.
+spark_status project_in(cublasLtHandle_t h, const void *x, const void *w_qkv, const void *w_g,
+                        long long rows, int hidden, int H, int Hkv, uint8_t *ws,
+                        const LayerPlan &pl, cudaStream_t stream) {
+    const int M = static_cast<int>(rows);
+    if (!linear(h, x, w_qkv, ws + pl.qkv, CUDA_R_16BF, M, (H + 2 * Hkv) * kHeadDim, hidden,
+                ws + pl.lt, stream) ||
+        !linear(h, x, w_g, ws + pl.gate, CUDA_R_32F, M, H, hidden, ws + pl.lt, stream))
+        return SPARK_ERR_CUDA;
+    const long long n = rows * H;
+    const cudaError_t e = launch_overlapped(round_gate_kernel,
+                                            dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256),
+                                            0, stream, reinterpret_cast<float *>(ws + pl.gate), n);
+    return e == cudaSuccess ? SPARK_OK : SPARK_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace spark
+
+using namespace spark;
+
+extern "C" {
+
+size_t spark_attn_layer_prefill_workspace_size(int B, int T, int hidden, int H, int Hkv,
+                                               const spark_layer_desc *desc) {
+    if (check_hidden(hidden) != SPARK_OK) return 0;
+    const size_t core = spark_attn_prefill_workspace_size(B, T, H, Hkv, desc);
+    if (core == 0) return 0;
+    return plan_layer(core, static_cast<long long>(B) * T, H, Hkv).bytes;
+}
+
+spark_status spark_attn_layer_prefill(const void *x, const void *w_qkv, const void *w_g,
+                                      const void *w_o, const int32_t *pos, void *k_cache,
+                                      void *v_cache, int64_t cap, const spark_layer_desc *desc,
+                                      int B, int T, int hidden, int H, int Hkv, void *y,
+                                      void *workspace, size_t workspace_bytes, void *stream) {
+    spark_status st = check_hidden(hidden);
+    if (st != SPARK_OK) return st;
+    const size_t core = spark_attn_prefill_workspace_size(B, T, H, Hkv, desc);
+    if (!desc) return SPARK_ERR_NULL;
+    if (core == 0) {
+        // the core's own checks name the problem
+        st = prefill_impl(nullptr, nullptr, nullptr, desc, B, T, H, Hkv, nullptr, nullptr, nullptr,
+                          0, nullptr, nullptr, 0, stream, true);
+        return st != SPARK_OK ? st : SPARK_ERR_SHAPE;
+    }
+    if (B == 0 || T == 0) return SPARK_OK;
+    if (!x || !w_qkv || !w_g || !w_o || !pos || !y || !workspace) return SPARK_ERR_NULL;
+    if ((k_cache == nullptr) != (v_cache == nullptr)) return SPARK_ERR_NULL;
+    if (!aligned16(x) || !aligned16(w_qkv) || !aligned16(w_g) || !aligned16(w_o) ||
+        !aligned16(y))
+        return SPARK_ERR_ALIGN;
+    const long long rows = static_cast<long long>(B) * T;
+    const LayerPlan pl = plan_layer(core, rows, H, Hkv);
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return SPARK_ERR_ALIGN;
+    if (workspace_bytes < pl.bytes) return SPARK_ERR_WORKSPACE;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    void *qkv = ws + pl.qkv, *attn = ws + pl.attn;
+    float *gate = reinterpret_cast<float *>(ws + pl.gate);
+    // every check of the core call below, before anything is enqueued
+    st = prefill_impl(qkv, gate, pos, desc, B, T, H, Hkv, attn, k_cache, v_cache, cap, nullptr,
+                      ws, core, stream, true);
+    if (st != SPARK_OK) return st;
+    cublasLtHandle_t h = lt_handle();
+    if (!h) return SPARK_ERR_CUDA;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = project_in(h, x, w_qkv, w_g, rows, hidden, H, Hkv, ws, pl, s);
+    if (st != SPARK_OK) return st;
+    st = prefill_impl(qkv, gate, pos, desc, B, T, H, Hkv, attn, k_cache, v_cache, cap, nullptr,
+                      ws, core, stream, false);
+    if (st != SPARK_OK) return st;
+    return linear(h, attn, w_o, y, CUDA_R_16BF, static_cast<int>(rows), hidden, H * kHeadDim,
+                  ws + pl.lt, s)
+               ? SPARK_OK
+               : SPARK_ERR_CUDA;
+}
+
+size_t spark_attn_layer_decode_workspace_size(int B, int hidden, int H, int Hkv, int64_t cap,
+                                              const spark_layer_desc *desc) {
+    if (check_hidden(hidden) != SPARK_OK) return 0;
+    const size_t core = spark_attn_decode_workspace_size(B, H, Hkv, cap, desc);
+    if (core == 0) return 0;
+    return plan_layer(core, B, H, Hkv).bytes;
+}
+
+spark_status spark_attn_layer_decode(const void *x, const void *w_qkv, const void *w_g,
+                                     const void *w_o, const int32_t *pos, void *k_cache,
+                                     void *v_cache, int64_t cap, const spark_layer_desc *desc,
+                                     int B, int hidden, int H, int Hkv, void *y, void *workspace,
+                                     size_t workspace_bytes, void *stream) {
+    spark_status st = check_hidden(hidden);
+    if (st != SPARK_OK) return st;
+    if (!desc) return SPARK_ERR_NULL;
+    const size_t core = spark_attn_decode_workspace_size(B, H, Hkv, cap, desc);
+    if (core == 0) {
+        st = decode_impl(nullptr, nullptr, nullptr, nullptr, nullptr, cap, desc, B, H, Hkv,
+                         nullptr, nullptr, 0, stream, true);
+        return st != SPARK_OK ? st : SPARK_ERR_SHAPE;
+    }
+    if (B == 0) return SPARK_OK;
+    if (!x || !w_qkv || !w_g || !w_o || !pos || !k_cache || !v_cache || !y || !workspace)
+        return SPARK_ERR_NULL;
+    if (!aligned16(x) || !aligned16(w_qkv) || !aligned16(w_g) || !aligned16(w_o) ||
+        !aligned16(y))
+        return SPARK_ERR_ALIGN;
+    const LayerPlan pl = plan_layer(core, B, H, Hkv);
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return SPARK_ERR_ALIGN;
+    if (workspace_bytes < pl.bytes) return SPARK_ERR_WORKSPACE;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    void *qkv = ws + pl.qkv, *attn = ws + pl.attn;
+    float *gate = reinterpret_cast<float *>(ws + pl.gate);
+    st = decode_impl(qkv, gate, pos, k_cache, v_cache, cap, desc, B, H, Hkv, attn, ws, core,
+                     stream, true);
+    if (st != SPARK_OK) return st;
+    cublasLtHandle_t h = lt_handle();
+    if (!h) return SPARK_ERR_CUDA;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = project_in(h, x, w_qkv, w_g, B, hidden, H, Hkv, ws, pl, s);
+    if (st != SPARK_OK) return st;
+    st = decode_impl(qkv, gate, pos, k_cache, v_cache, cap, desc, B, H, Hkv, attn, ws, core,
+                     stream, false);
+    if (st != SPARK_OK) return st;
+    return linear(h, attn, w_o, y, CUDA_R_16BF, B, hidden, H * kHeadDim, ws + pl.lt, s)
+               ? SPARK_OK
+               : SPARK_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -226,12 +226,16 @@ spark_status check_prefill(int B, int T, int H, int Hkv, const spark_layer_desc 
     return SPARK_OK;
 }
 
+}  // namespace
+
 // Prefill, optionally filling the decode cache (k_cache != nullptr), or a
-// chunked prefill over a cache that already holds start[b] tokens.
+// chunked prefill over a cache that already holds start[b] tokens.  With
+// validate_only, returns after the host-side checks and enqueues nothing.
 spark_status prefill_impl(const void *qkv, const float *gate, const int32_t *pos,
                           const spark_layer_desc *desc, int B, int T, int H, int Hkv, void *out,
                           void *k_cache, void *v_cache, int64_t cap, const int32_t *start,
-                          void *workspace, size_t workspace_bytes, void *stream) {
+                          void *workspace, size_t workspace_bytes, void *stream,
+                          bool validate_only) {
     spark_status st = check_prefill(B, T, H, Hkv, desc);
     if (st != SPARK_OK) return st;
     if (k_cache || v_cache) {
@@ -255,7 +259,7 @@ spark_status prefill_impl(const void *qkv, const float *gate, const int32_t *pos
     const PrefillPlan pl = plan_prefill(B, T, Hkv, desc);
     if (workspace_bytes < pl.bytes) return SPARK_ERR_WORKSPACE;
     st = check_device();
-    if (st != SPARK_OK) return st;
+    if (st != SPARK_OK || validate_only) return st;
 
     const int G = H / Hkv;
     const int tq = kPrefillRows / G;  // tokens per query tile
@@ -343,40 +347,11 @@ spark_status prefill_impl(const void *qkv, const float *gate, const int32_t *pos
                                     static_cast<cudaStream_t>(stream)));
 }
 
-}  // namespace
-}  // namespace spark
-
-using namespace spark;
-
-extern "C" {
-
-const char *spark_status_str(spark_status s) {
-    switch (s) {
-        case SPARK_OK: return "ok";
-        case SPARK_ERR_NULL: return "a required pointer is NULL";
-        case SPARK_ERR_SHAPE: return "a size is negative or inconsistent";
-        case SPARK_ERR_UNSUPPORTED: return "valid arguments that this build does not support";
-        case SPARK_ERR_ALIGN: return "a pointer is not aligned (16 bytes; workspace 256 bytes)";
-        case SPARK_ERR_CAPACITY: return "the KV cache is too small for the layer";
-        case SPARK_ERR_WORKSPACE: return "workspace missing or too small";
-        case SPARK_ERR_CUDA: return "a CUDA call failed while enqueuing work";
-        case SPARK_ERR_DEVICE: return "the current device is not an sm_103 GPU";
-    }
-    return "unknown status";
-}
-
-const char *spark_attn_version(void) { return "0.1.0"; }
-
-size_t spark_attn_decode_workspace_size(int B, int H, int Hkv, int64_t cap,
-                                        const spark_layer_desc *desc) {
-    if (check_decode(B, H, Hkv, cap, desc) != SPARK_OK) return 0;
-    return plan_decode(B, H, Hkv, cap, desc, sm_count_or_default()).bytes;
-}
-
-spark_status spark_attn_decode(const void *qkv, const float *gate, const int32_t *pos,
-                               void *k_cache, void *v_cache, int64_t cap,
-                               const spark_layer_desc *desc, int B, int H, int Hkv, void *out,
-                               void *workspace, size_t workspace_bytes, void *stream) {
+// One decode step; with validate_only, returns after the host-side checks.
+spark_status decode_impl(const void *qkv, const float *gate, const int32_t *pos, void *k_cache,
+                         void *v_cache, int64_t cap, const spark_layer_desc *desc, int B, int H,
+                         int Hkv, void *out, void *workspace, size_t workspace_bytes,
+                         void *stream, bool validate_only) {
     spark_status st = check_decode(B, H, Hkv, cap, desc);
     if (st != SPARK_OK) return st;
     if (B == 0) return SPARK_OK;
@@ -387,7 +362,7 @@ spark_status spark_attn_decode(const void *qkv, const float *gate, const int32_t
     const DecodePlan pl = plan_decode(B, H, Hkv, cap, desc, sm_count_or_default());
     if (workspace_bytes < pl.bytes) return SPARK_ERR_WORKSPACE;
     st = check_device();
-    if (st != SPARK_OK) return st;
+    if (st != SPARK_OK || validate_only) return st;
 
     DecodeParams P;
     std::memset(&P, 0, sizeof(P));
@@ -426,6 +401,43 @@ spark_status spark_attn_decode(const void *qkv, const float *gate, const int32_t
     return from_cuda(launch_decode(tm_k, tm_v, P, static_cast<cudaStream_t>(stream)));
 }
 
+}  // namespace spark
+
+using namespace spark;
+
+extern "C" {
+
+const char *spark_status_str(spark_status s) {
+    switch (s) {
+        case SPARK_OK: return "ok";
+        case SPARK_ERR_NULL: return "a required pointer is NULL";
+        case SPARK_ERR_SHAPE: return "a size is negative or inconsistent";
+        case SPARK_ERR_UNSUPPORTED: return "valid arguments that this build does not support";
+        case SPARK_ERR_ALIGN: return "a pointer is not aligned (16 bytes; workspace 256 bytes)";
+        case SPARK_ERR_CAPACITY: return "the KV cache is too small for the layer";
+        case SPARK_ERR_WORKSPACE: return "workspace missing or too small";
+        case SPARK_ERR_CUDA: return "a CUDA call failed while enqueuing work";
+        case SPARK_ERR_DEVICE: return "the current device is not an sm_103 GPU";
+    }
+    return "unknown status";
+}
+
+const char *spark_attn_version(void) { return "0.1.0"; }
+
+size_t spark_attn_decode_workspace_size(int B, int H, int Hkv, int64_t cap,
+                                        const spark_layer_desc *desc) {
+    if (check_decode(B, H, Hkv, cap, desc) != SPARK_OK) return 0;
+    return plan_decode(B, H, Hkv, cap, desc, sm_count_or_default()).bytes;
+}
+
+spark_status spark_attn_decode(const void *qkv, const float *gate, const int32_t *pos,
+                               void *k_cache, void *v_cache, int64_t cap,
+                               const spark_layer_desc *desc, int B, int H, int Hkv, void *out,
+                               void *workspace, size_t workspace_bytes, void *stream) {
+    return decode_impl(qkv, gate, pos, k_cache, v_cache, cap, desc, B, H, Hkv, out, workspace,
+                       workspace_bytes, stream, false);
+}
+
 size_t spark_attn_prefill_workspace_size(int B, int T, int H, int Hkv,
                                          const spark_layer_desc *desc) {
     if (check_prefill(B, T, H, Hkv, desc) != SPARK_OK) return 0;
@@ -437,7 +449,7 @@ extern "C" spark_status spark_attn_prefill(const void *qkv, const float *gate, c
                                            int Hkv, void *out, void *workspace,
                                            size_t workspace_bytes, void *stream) {
     return prefill_impl(qkv, gate, pos, desc, B, T, H, Hkv, out, nullptr, nullptr, 0, nullptr,
-                        workspace, workspace_bytes, stream);
+                        workspace, workspace_bytes, stream, false);
 }
 
 extern "C" spark_status spark_attn_prefill_cache(const void *qkv, const float *gate,
@@ -451,7 +463,7 @@ extern "C" spark_status spark_attn_prefill_cache(const void *qkv, const float *g
     if (B == 0 || T == 0) return SPARK_OK;
     if (!k_cache || !v_cache) return SPARK_ERR_NULL;
     return prefill_impl(qkv, gate, pos, desc, B, T, H, Hkv, out, k_cache, v_cache, cap, nullptr,
-                        workspace, workspace_bytes, stream);
+                        workspace, workspace_bytes, stream, false);
 }
 
 extern "C" spark_status spark_attn_prefill_chunk(const void *qkv, const float *gate,
@@ -466,7 +478,7 @@ extern "C" spark_status spark_attn_prefill_chunk(const void *qkv, const float *g
     if (B == 0 || T == 0) return SPARK_OK;
     if (!k_cache || !v_cache || !start) return SPARK_ERR_NULL;
     return prefill_impl(qkv, gate, pos, desc, B, T, H, Hkv, out, k_cache, v_cache, cap, start,
-                        workspace, workspace_bytes, stream);
+                        workspace, workspace_bytes, stream, false);
 }
 
 spark_status spark_attn_read_status(void *workspace, uint32_t *status_out, int clear,

@@ -41,7 +41,8 @@
  *  - All data pointers are DEVICE pointers of the current CUDA device, 16-byte
  *    aligned, dense row-major in the stated layout.  The caller owns every
  *    buffer; the library allocates no device memory and keeps no per-call
- *    state between calls.
+ *    state between calls (the layer calls keep one cuBLASLt handle per
+ *    device).
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *    stream) and runs asynchronously; nothing synchronizes.
  *  - Argument errors are found on the host before anything is enqueued; the
@@ -231,6 +232,55 @@ spark_status spark_attn_decode_noalloc(const void *qkv, const float *gate, const
                                        void *k_cache, void *v_cache, int64_t cap,
                                        const spark_layer_desc *desc, int B, int H, int Hkv,
                                        void *out, uint32_t *device_status, void *stream);
+
+/*
+ * The attention block around the core (Spark-X2.5 architecture, §3 Eq. 1 and
+ * Fig. 1): q_k_v_proj and g_proj read the normed hidden state x, the core
+ * attends, out_proj maps the gated output back to the hidden size:
+ *
+ *   qkv  = bf16( x W_qkv^T )      W_qkv bf16 [(H + 2*Hkv) * 256, hidden]
+ *   g    = bf16( x W_g^T )        W_g   bf16 [H, hidden]   (one logit per head)
+ *   a    = core(qkv, g, pos)      as spark_attn_prefill / spark_attn_decode
+ *   y    = bf16( a W_o^T )        W_o   bf16 [hidden, H * 256]
+ *
+ * Weights use the PyTorch Linear layout (out_features x in_features, row
+ * major); there are no biases.  Every product accumulates in fp32 and rounds
+ * once to bf16 (the checkpoints' dtype, §1); the residual add and the norms
+ * stay outside.  The projections are dense GEMMs and run through cuBLASLt on
+ * `stream` (one cuBLASLt handle per device, created on the first call), with
+ * the caller's workspace as its scratch.  hidden must be a positive multiple
+ * of 8 (16-byte rows; else SPARK_ERR_UNSUPPORTED).
+ *
+ * Prefill:
+ *   x  bf16 [B, T, hidden];  pos int32 [B, T];  y bf16 [B, T, hidden]
+ *   k_cache, v_cache, cap: optional (both NULL, cap ignored) -- when given,
+ *            the call also fills the decode cache as spark_attn_prefill_cache
+ *            does (same capacity rules).
+ * Decode (one new token per sequence):
+ *   x  bf16 [B, hidden];  pos int32 [B];  y bf16 [B, hidden]
+ *   k_cache, v_cache, cap as for spark_attn_decode (required).
+ * workspace: >= the size query's bytes, 256-byte aligned, zeroed once before
+ * first use; its status word (spark_attn_read_status) is the core's.  Every
+ * argument, including the core's, is checked before anything is enqueued.
+ * The size queries return 0 for invalid arguments.
+ */
+size_t spark_attn_layer_prefill_workspace_size(int B, int T, int hidden, int H, int Hkv,
+                                               const spark_layer_desc *desc);
+
+spark_status spark_attn_layer_prefill(const void *x, const void *w_qkv, const void *w_g,
+                                      const void *w_o, const int32_t *pos, void *k_cache,
+                                      void *v_cache, int64_t cap, const spark_layer_desc *desc,
+                                      int B, int T, int hidden, int H, int Hkv, void *y,
+                                      void *workspace, size_t workspace_bytes, void *stream);
+
+size_t spark_attn_layer_decode_workspace_size(int B, int hidden, int H, int Hkv, int64_t cap,
+                                              const spark_layer_desc *desc);
+
+spark_status spark_attn_layer_decode(const void *x, const void *w_qkv, const void *w_g,
+                                     const void *w_o, const int32_t *pos, void *k_cache,
+                                     void *v_cache, int64_t cap, const spark_layer_desc *desc,
+                                     int B, int hidden, int H, int Hkv, void *y, void *workspace,
+                                     size_t workspace_bytes, void *stream);
 
 /*
  * Copies the sticky device status word out of a workspace (synchronizes on

@@ -133,3 +133,37 @@ def test_binding_refuses_cpu_tensors():
     with pytest.raises(TypeError):
         fga.spark_attn_prefill(x, torch.zeros((1, 4, 4)), torch.zeros((1, 4), dtype=torch.int32),
                                fga.layer_desc(0, 0, 5e6, 64))
+
+
+def test_layer_calls_check_before_enqueueing():
+    """The attention-block calls refuse bad arguments on the host (no GPU is
+    needed to reach these answers)."""
+    full = fga.layer_desc(fga.SPARK_LAYER_FULL, 0, 5e6, 64)
+    d = ctypes.byref(full)
+    L = fga.lib
+    # hidden not a multiple of 8, or not positive
+    assert L.spark_attn_layer_prefill(None, None, None, None, None, None, None, 0, d, 1, 4, 2561,
+                                      16, 4, None, None, 0, None) == 3
+    assert L.spark_attn_layer_prefill(None, None, None, None, None, None, None, 0, d, 1, 4, 0,
+                                      16, 4, None, None, 0, None) == 2
+    # the core's own shape rule (H % Hkv)
+    assert L.spark_attn_layer_prefill(None, None, None, None, None, None, None, 0, d, 1, 4, 2560,
+                                      16, 3, None, None, 0, None) == 2
+    assert L.spark_attn_layer_decode(None, None, None, None, None, None, None, 100, d, 1, 2560,
+                                     16, 3, None, None, 0, None) == 2
+    # empty batch: nothing to do
+    assert L.spark_attn_layer_prefill(None, None, None, None, None, None, None, 0, d, 0, 4, 2560,
+                                      16, 4, None, None, 0, None) == 0
+    assert L.spark_attn_layer_decode(None, None, None, None, None, None, None, 100, d, 0, 2560,
+                                     16, 4, None, None, 0, None) == 0
+    # missing pointers
+    assert L.spark_attn_layer_prefill(None, None, None, None, None, None, None, 0, d, 1, 4, 2560,
+                                      16, 4, None, None, 0, None) == 1
+    # workspace sizes: the core's plus the projections' buffers
+    core = L.spark_attn_prefill_workspace_size(2, 8192, 16, 4, d)
+    n = L.spark_attn_layer_prefill_workspace_size(2, 8192, 2560, 16, 4, d)
+    rows = 2 * 8192
+    assert n >= core + rows * (6144 * 2 + 16 * 4 + 4096 * 2)
+    assert L.spark_attn_layer_prefill_workspace_size(2, 8192, 2561, 16, 4, d) == 0
+    assert L.spark_attn_layer_decode_workspace_size(1, 2560, 16, 4, 1 << 20, d) > \
+        L.spark_attn_decode_workspace_size(1, 16, 4, 1 << 20, d)
