@@ -7,7 +7,9 @@ One step is one pass of the whole hot path over one batch of synthetic input:
     layer order (9 full layers with 1,048,575 cached tokens each, 27 sliding
     layers with full 512-slot rings): 38.71 GB of KV read.
 The JSON line's value is the prefill throughput (TFLOP/s); the decode KV-read
-bandwidth is reported beside it.  Inputs are seeded synthetic tensors of the
+bandwidth is reported beside it.  Outside the timed step the line also carries
+the 1.7B sliding prefill (B=1, T=1024) per call and in a CUDA graph, and the
+whole attention block of the prefill layer (projections + core).  Inputs are seeded synthetic tensors of the
 model's shapes (no dataset or weights exist for this path).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {ours,reference}]
@@ -424,6 +426,7 @@ def run_ours(args, rank, world, local):
     }
     if pre is not None and rank == 0:
         line["small_prefill"] = time_small_prefill(fga, dev, bf16_peak)
+        line["layer_prefill"] = time_layer_prefill(fga, dev, bf16_peak)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args)
     return line
@@ -483,6 +486,55 @@ def time_small_prefill(fga, dev, bf16_peak, calls=50):
         "tflops_graph": flops / graph_ms / 1e9,
         "frac_bf16_peak_graph": flops / graph_ms / 1e9 / bf16_peak,
         "device_status": status,
+    }
+
+
+def time_layer_prefill(fga, dev, bf16_peak, calls=10):
+    """The whole attention block of the benchmark's prefill layer (4B
+    full_attention, B=2, T=8192, hidden 2560): q_k_v_proj and g_proj
+    (cuBLASLt), the core, out_proj (cuBLASLt), with seeded random weights of
+    the model's shapes.  Work = the three projections' flops plus the core's
+    algorithmic flops."""
+    import torch
+    c = PREFILL
+    hidden = 2560
+    g = torch.Generator().manual_seed(11)
+    x = torch.randn((c.B, c.T, hidden), generator=g).to(torch.bfloat16).to(dev)
+    width = (c.H + 2 * c.Hkv) * 256
+    w_qkv = (torch.randn((width, hidden), generator=g) / hidden ** 0.5).to(torch.bfloat16).to(dev)
+    w_g = (torch.randn((c.H, hidden), generator=g) / hidden ** 0.5).to(torch.bfloat16).to(dev)
+    w_o = (torch.randn((hidden, c.H * 256), generator=g) / (c.H * 256) ** 0.5).to(
+        torch.bfloat16).to(dev)
+    pos = torch.arange(c.T, dtype=torch.int32, device=dev).repeat(c.B, 1)
+    y = torch.empty((c.B, c.T, hidden), dtype=torch.bfloat16, device=dev)
+    ws = fga.new_workspace(fga.spark_attn_layer_prefill_workspace_size(c.B, c.T, hidden, c.H,
+                                                                       c.Hkv, c.layer), dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        fga.spark_attn_layer_prefill(x, w_qkv, w_g, w_o, pos, c.layer, y=y, workspace=ws,
+                                     stream=stream)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(calls):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / calls
+    rows = c.B * c.T
+    proj = 2.0 * rows * hidden * (width + c.H + c.H * 256)
+    flops = proj + prefill_flops(c)
+    return {
+        "workload": "attention block of the prefill layer: q_k_v_proj 2560->6144, g_proj "
+                    "2560->16, core, out_proj 4096->2560 (4B, B=2 T=8192, random weights)",
+        "ms": ms, "flops": flops, "projection_flops": proj,
+        "tflops": flops / ms / 1e9, "frac_bf16_peak": flops / ms / 1e9 / bf16_peak,
+        "calls": calls, "projections": "cuBLASLt bf16 GEMMs, fp32 accumulation",
+        "device_status": fga.spark_attn_read_status(ws),
     }
 
 

@@ -14,7 +14,9 @@
 // before the core's epilogue takes sigmoid of it in fp32.
 #include <cublasLt.h>
 
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "common.cuh"
 #include "spark_attn.h"
@@ -59,24 +61,50 @@ cublasLtHandle_t lt_handle() {
 // y[M, N] = x[M, K] * W[N, K]^T: row-major bf16 x and W (a PyTorch Linear
 // weight), y bf16 or fp32 row-major, fp32 accumulation.  In cuBLAS's
 // column-major terms: y^T (N x M) = W (stored K x N, transposed) * x^T (K x M).
-bool linear(cublasLtHandle_t h, const void *x, const void *w, void *y, cudaDataType_t y_type,
-            int M, int N, int K, void *lt_ws, cudaStream_t stream) {
+// The descriptors and the algorithm cuBLASLt's heuristic picks are kept per
+// (device, M, N, K, output type), so repeated calls skip the host-side set-up.
+struct LinearPlan {
     cublasLtMatmulDesc_t op = nullptr;
     cublasLtMatrixLayout_t la = nullptr, lb = nullptr, lc = nullptr;
-    cublasLtMatmulPreference_t pref = nullptr;
+    cublasLtMatmulAlgo_t algo;
     bool ok = false;
+};
+
+struct PlanKey {
+    int dev, M, N, K, y_type;
+    bool operator<(const PlanKey &o) const {
+        return std::tie(dev, M, N, K, y_type) < std::tie(o.dev, o.M, o.N, o.K, o.y_type);
+    }
+};
+
+constexpr size_t kMaxPlans = 256;
+std::mutex g_plan_mu;
+std::map<PlanKey, LinearPlan> g_plans;
+
+void destroy_plan(LinearPlan &p) {
+    if (p.lc) cublasLtMatrixLayoutDestroy(p.lc);
+    if (p.lb) cublasLtMatrixLayoutDestroy(p.lb);
+    if (p.la) cublasLtMatrixLayoutDestroy(p.la);
+    if (p.op) cublasLtMatmulDescDestroy(p.op);
+    p = LinearPlan();
+}
+
+LinearPlan make_plan(cublasLtHandle_t h, cudaDataType_t y_type, int M, int N, int K) {
+    LinearPlan p;
+    cublasLtMatmulPreference_t pref = nullptr;
     do {
-        if (cublasLtMatmulDescCreate(&op, CUBLAS_COMPUTE_32F, CUDA_R_32F) != CUBLAS_STATUS_SUCCESS)
+        if (cublasLtMatmulDescCreate(&p.op, CUBLAS_COMPUTE_32F, CUDA_R_32F) !=
+            CUBLAS_STATUS_SUCCESS)
             break;
         const cublasOperation_t ta = CUBLAS_OP_T, tb = CUBLAS_OP_N;
-        if (cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSA, &ta, sizeof(ta)) !=
+        if (cublasLtMatmulDescSetAttribute(p.op, CUBLASLT_MATMUL_DESC_TRANSA, &ta, sizeof(ta)) !=
                 CUBLAS_STATUS_SUCCESS ||
-            cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSB, &tb, sizeof(tb)) !=
+            cublasLtMatmulDescSetAttribute(p.op, CUBLASLT_MATMUL_DESC_TRANSB, &tb, sizeof(tb)) !=
                 CUBLAS_STATUS_SUCCESS)
             break;
-        if (cublasLtMatrixLayoutCreate(&la, CUDA_R_16BF, K, N, K) != CUBLAS_STATUS_SUCCESS ||
-            cublasLtMatrixLayoutCreate(&lb, CUDA_R_16BF, K, M, K) != CUBLAS_STATUS_SUCCESS ||
-            cublasLtMatrixLayoutCreate(&lc, y_type, N, M, N) != CUBLAS_STATUS_SUCCESS)
+        if (cublasLtMatrixLayoutCreate(&p.la, CUDA_R_16BF, K, N, K) != CUBLAS_STATUS_SUCCESS ||
+            cublasLtMatrixLayoutCreate(&p.lb, CUDA_R_16BF, K, M, K) != CUBLAS_STATUS_SUCCESS ||
+            cublasLtMatrixLayoutCreate(&p.lc, y_type, N, M, N) != CUBLAS_STATUS_SUCCESS)
             break;
         if (cublasLtMatmulPreferenceCreate(&pref) != CUBLAS_STATUS_SUCCESS) break;
         const size_t ws_bytes = kLtWorkspace;
@@ -86,20 +114,44 @@ bool linear(cublasLtHandle_t h, const void *x, const void *w, void *y, cudaDataT
             break;
         cublasLtMatmulHeuristicResult_t res;
         int found = 0;
-        if (cublasLtMatmulAlgoGetHeuristic(h, op, la, lb, lc, lc, pref, 1, &res, &found) !=
-                CUBLAS_STATUS_SUCCESS ||
+        if (cublasLtMatmulAlgoGetHeuristic(h, p.op, p.la, p.lb, p.lc, p.lc, pref, 1, &res,
+                                           &found) != CUBLAS_STATUS_SUCCESS ||
             found < 1)
             break;
-        const float alpha = 1.0f, beta = 0.0f;
-        ok = cublasLtMatmul(h, op, &alpha, w, la, x, lb, &beta, y, lc, y, lc, &res.algo, lt_ws,
-                            ws_bytes, stream) == CUBLAS_STATUS_SUCCESS;
+        p.algo = res.algo;
+        p.ok = true;
     } while (false);
     if (pref) cublasLtMatmulPreferenceDestroy(pref);
-    if (lc) cublasLtMatrixLayoutDestroy(lc);
-    if (lb) cublasLtMatrixLayoutDestroy(lb);
-    if (la) cublasLtMatrixLayoutDestroy(la);
-    if (op) cublasLtMatmulDescDestroy(op);
-    return ok;
+    if (!p.ok) destroy_plan(p);
+    return p;
+}
+
+bool linear(cublasLtHandle_t h, const void *x, const void *w, void *y, cudaDataType_t y_type,
+            int M, int N, int K, void *lt_ws, cudaStream_t stream) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const PlanKey key{dev, M, N, K, static_cast<int>(y_type)};
+    const float alpha = 1.0f, beta = 0.0f;
+    std::unique_lock<std::mutex> lock(g_plan_mu);
+    auto it = g_plans.find(key);
+    if (it == g_plans.end()) {
+        LinearPlan p = make_plan(h, y_type, M, N, K);
+        if (!p.ok) return false;
+        if (g_plans.size() >= kMaxPlans) {
+            // too many shapes to keep: run this one and drop its plan
+            lock.unlock();
+            const bool ok = cublasLtMatmul(h, p.op, &alpha, w, p.la, x, p.lb, &beta, y, p.lc, y,
+                                           p.lc, &p.algo, lt_ws, kLtWorkspace,
+                                           stream) == CUBLAS_STATUS_SUCCESS;
+            destroy_plan(p);
+            return ok;
+        }
+        it = g_plans.emplace(key, p).first;
+    }
+    const LinearPlan p = it->second;  // plans are never destroyed once stored
+    lock.unlock();
+    return cublasLtMatmul(h, p.op, &alpha, w, p.la, x, p.lb, &beta, y, p.lc, y, p.lc, &p.algo,
+                          lt_ws, kLtWorkspace, stream) == CUBLAS_STATUS_SUCCESS;
 }
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
