@@ -68,6 +68,10 @@ def _load() -> ctypes.CDLL:
     lib.spark_attn_decode.restype = i32
     lib.spark_attn_decode_noalloc.argtypes = [P, P, P, P, P, i64, D, i32, i32, i32, P, P, P]
     lib.spark_attn_decode_noalloc.restype = i32
+    lib.spark_attn_prefill_host_workspace_size.argtypes = [i32, i32, i32, i32, D]
+    lib.spark_attn_prefill_host_workspace_size.restype = sz
+    lib.spark_attn_prefill_host.argtypes = [P, P, P, D, i32, i32, i32, i32, P, P, sz, P]
+    lib.spark_attn_prefill_host.restype = i32
     lib.spark_attn_layer_prefill_workspace_size.argtypes = [i32, i32, i32, i32, i32, D]
     lib.spark_attn_layer_prefill_workspace_size.restype = sz
     lib.spark_attn_layer_prefill.argtypes = [P, P, P, P, P, P, P, i64, D, i32, i32, i32, i32,
@@ -351,6 +355,51 @@ def spark_attn_decode_noalloc(qkv: torch.Tensor, gate: torch.Tensor, pos: torch.
                                        Hkv, _ptr(out), _ptr(device_status), _stream(stream))
     if st != SPARK_OK:
         raise SparkError(st, "spark_attn_decode_noalloc")
+    return out
+
+
+def _need_host(t: torch.Tensor, dtype, name: str):
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or t.is_cuda:
+        raise TypeError(f"{name} must be a host (CPU) {dtype} tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def spark_attn_prefill_host_workspace_size(B: int, T: int, H: int, Hkv: int, layer) -> int:
+    d = as_desc(layer)
+    return lib.spark_attn_prefill_host_workspace_size(B, T, H, Hkv, ctypes.byref(d))
+
+
+def spark_attn_prefill_host(qkv: torch.Tensor, gate: torch.Tensor, pos: torch.Tensor, layer,
+                            out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                            stream=None, device=None) -> torch.Tensor:
+    """Prefill of HOST tensors (pin them for overlapped copies): qkv bf16
+    [B,T,(H+2Hkv)*256], gate fp32 [B,T,H], pos int32 [B,T] -> out bf16
+    [B,T,H*256] in host memory.  The copies of one sequence overlap the
+    compute of another; synchronize `stream` before reading `out`."""
+    _need_host(qkv, torch.bfloat16, "qkv")
+    _need_host(gate, torch.float32, "gate")
+    _need_host(pos, torch.int32, "pos")
+    B, T, W = qkv.shape
+    H = gate.shape[-1]
+    Hkv = (W // HEAD_DIM - H) // 2
+    if gate.shape != (B, T, H) or pos.shape != (B, T) or (H + 2 * Hkv) * HEAD_DIM != W:
+        raise ValueError("inconsistent prefill shapes")
+    d = as_desc(layer)
+    if out is None:
+        out = torch.empty((B, T, H * HEAD_DIM), dtype=torch.bfloat16, pin_memory=qkv.is_pinned())
+    _need_host(out, torch.bfloat16, "out")
+    need = lib.spark_attn_prefill_host_workspace_size(B, T, H, Hkv, ctypes.byref(d))
+    owned = workspace is None
+    if owned:
+        workspace = new_workspace(need, device)
+    st = lib.spark_attn_prefill_host(_ptr(qkv), _ptr(gate), _ptr(pos), ctypes.byref(d), B, T, H,
+                                     Hkv, _ptr(out), _ptr(workspace), workspace.numel(),
+                                     _stream(stream))
+    if st != SPARK_OK:
+        raise SparkError(st, "spark_attn_prefill_host")
+    if owned:
+        _check_owned(workspace, "spark_attn_prefill_host", stream)
     return out
 
 

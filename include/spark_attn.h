@@ -38,8 +38,9 @@
  * RoPE angles are reduced exactly in fp32 (positions below 2^24).
  *
  * Conventions for every entry point:
- *  - All data pointers are DEVICE pointers of the current CUDA device, 16-byte
- *    aligned, dense row-major in the stated layout.  The caller owns every
+ *  - All data pointers are DEVICE pointers of the current CUDA device (except
+ *    the host buffers of spark_attn_prefill_host), 16-byte aligned, dense
+ *    row-major in the stated layout.  The caller owns every
  *    buffer; the library allocates no device memory and keeps no per-call
  *    state between calls (the layer calls keep one cuBLASLt handle per
  *    device).
@@ -123,6 +124,35 @@ spark_status spark_attn_prefill(const void *qkv, const float *gate, const int32_
                                 const spark_layer_desc *desc, int B, int T, int H, int Hkv,
                                 void *out, void *workspace, size_t workspace_bytes,
                                 void *stream);
+
+/*
+ * Prefill from and to HOST memory.  Computes exactly what spark_attn_prefill
+ * computes, for inputs and outputs that live in host memory:
+ *
+ *   qkv_h, gate_h, pos_h   HOST pointers, layouts as for spark_attn_prefill
+ *   out_h                  HOST pointer, bf16 [B, T, H * 256]
+ *   workspace  DEVICE, >= spark_attn_prefill_host_workspace_size(...) bytes,
+ *              256-byte aligned, zeroed once before first use (its status word
+ *              is read with spark_attn_read_status)
+ *
+ * The batch goes through two device staging areas one sequence at a time:
+ * the copy-in of sequence b+1 and the copy-out of sequence b-1 run on two
+ * copy streams that the library creates per device on first use, while
+ * `stream` computes sequence b.  Host buffers should be pinned
+ * (cudaHostAlloc / cudaHostRegister); pageable memory still works, with
+ * copies that do not overlap.  The call returns once everything is enqueued:
+ * synchronize `stream` before reading out_h (work enqueued on `stream` after
+ * the call is ordered after the last copy-out).  Inputs must stay unchanged
+ * until then.  If a CUDA call fails part-way, SPARK_ERR_CUDA is returned
+ * and some sequences may have been processed.
+ */
+size_t spark_attn_prefill_host_workspace_size(int B, int T, int H, int Hkv,
+                                              const spark_layer_desc *desc);
+
+spark_status spark_attn_prefill_host(const void *qkv_h, const float *gate_h, const int32_t *pos_h,
+                                     const spark_layer_desc *desc, int B, int T, int H, int Hkv,
+                                     void *out_h, void *workspace, size_t workspace_bytes,
+                                     void *stream);
 
 /*
  * Prefill that also fills the decode cache: computes exactly what

@@ -1,0 +1,56 @@
+"""GPU tests of the prefill from and to host memory (spark_attn_prefill_host).
+
+It runs the same kernels as spark_attn_prefill, one sequence at a time, with
+the copies of one sequence overlapping the compute of another; its output must
+equal the device-memory call's bit for bit, for pinned and pageable buffers,
+with odd batch sizes that reuse the two staging areas.
+"""
+from __future__ import annotations
+
+import pytest
+import torch
+
+import full_gqa_attention_gb300 as fga
+import oracle
+import workloads as wl
+from parity import check_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("layer", [wl.FULL_LAYER, wl.SLIDING_LAYER], ids=["full", "sliding"])
+@pytest.mark.parametrize("B,T", [(1, 129), (3, 300), (5, 64)])
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+def test_host_prefill_equals_device_prefill(cuda, layer, B, T, pinned):
+    case = wl.PrefillCase("h", B=B, T=T, H=16, Hkv=4, layer=layer, seed=50 + B)
+    x = wl.make_prefill_inputs(case)
+    host = {k: (v.pin_memory() if pinned else v.clone()) for k, v in x.items()}
+    want = fga.spark_attn_prefill(x["qkv"].to(cuda), x["gate"].to(cuda), x["pos"].to(cuda), layer)
+    ws = fga.new_workspace(fga.spark_attn_prefill_host_workspace_size(B, T, 16, 4, layer))
+    got = fga.spark_attn_prefill_host(host["qkv"], host["gate"], host["pos"], layer, workspace=ws)
+    torch.cuda.synchronize()
+    assert fga.spark_attn_read_status(ws) == 0
+    assert torch.equal(got, want.cpu())
+
+
+def test_host_prefill_matches_the_oracle(cuda):
+    case = wl.PrefillCase("h", B=2, T=200, H=8, Hkv=2, layer=wl.SLIDING_LAYER, seed=61)
+    x = wl.make_prefill_inputs(case)
+    got = fga.spark_attn_prefill_host(x["qkv"].pin_memory(), x["gate"].pin_memory(),
+                                      x["pos"].pin_memory(), case.layer)
+    torch.cuda.synchronize()
+    L = case.layer
+    want = oracle.prefill(wl.bf16_bits(x["qkv"]), x["gate"].numpy(), x["pos"].numpy(), L.kind,
+                          L.window, L.theta, L.rot_dim, 8, 2)
+    check_close(got.reshape(400, -1), want.reshape(400, -1), "host prefill")
+
+
+def test_host_prefill_empty_and_rejects(cuda):
+    layer = wl.FULL_LAYER
+    e = torch.empty((0, 4, 6144), dtype=torch.bfloat16)
+    out = fga.spark_attn_prefill_host(e, torch.empty((0, 4, 16)), torch.empty((0, 4),
+                                      dtype=torch.int32), layer)
+    assert out.shape == (0, 4, 4096)
+    with pytest.raises(TypeError):
+        fga.spark_attn_prefill_host(e.to(cuda), torch.empty((0, 4, 16)),
+                                    torch.empty((0, 4), dtype=torch.int32), layer)
