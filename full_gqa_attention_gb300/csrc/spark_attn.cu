@@ -412,7 +412,7 @@ const char *spark_status_str(spark_status s) {
         case SPARK_OK: return "ok";
         case SPARK_ERR_NULL: return "a required pointer is NULL";
         case SPARK_ERR_SHAPE: return "a size is negative or inconsistent";
-        case SPARK_ERR_UNSUPPORTED: return "valid arguments that this build does not support";
+        case SPARK_ERR_UNSUPPORTED: return "valid arguments that the library does not support";
         case SPARK_ERR_ALIGN: return "a pointer is not aligned (16 bytes; workspace 256 bytes)";
         case SPARK_ERR_CAPACITY: return "the KV cache is too small for the layer";
         case SPARK_ERR_WORKSPACE: return "workspace missing or too small";
