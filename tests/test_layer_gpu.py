@@ -27,10 +27,10 @@ def bits(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().view(torch.int16).numpy().astype(np.uint16)
 
 
-def weights(hidden: int, H: int, Hkv: int, seed: int):
+def weights(hidden: int, H: int, Hkv: int, seed: int, gate_scale: float = 1.0):
     g = torch.Generator().manual_seed(seed)
     w_qkv = (torch.randn(((H + 2 * Hkv) * D, hidden), generator=g) / hidden ** 0.5)
-    w_g = (torch.randn((H, hidden), generator=g) / hidden ** 0.5)
+    w_g = (torch.randn((H, hidden), generator=g) * gate_scale / hidden ** 0.5)
     w_o = (torch.randn((hidden, H * D), generator=g) / (H * D) ** 0.5)
     return [w.to(torch.bfloat16) for w in (w_qkv, w_g, w_o)]
 
@@ -39,9 +39,9 @@ def hidden_states(shape, seed: int) -> torch.Tensor:
     return torch.randn(shape, generator=torch.Generator().manual_seed(seed)).to(torch.bfloat16)
 
 
-def run_prefill(cuda, B, T, hidden, H, Hkv, layer, seed, rows=None):
+def run_prefill(cuda, B, T, hidden, H, Hkv, layer, seed, rows=None, gate_scale=1.0):
     x = hidden_states((B, T, hidden), seed)
-    w = weights(hidden, H, Hkv, seed + 1)
+    w = weights(hidden, H, Hkv, seed + 1, gate_scale)
     pos = torch.arange(T, dtype=torch.int32).repeat(B, 1)
     ws = fga.new_workspace(fga.spark_attn_layer_prefill_workspace_size(B, T, hidden, H, Hkv,
                                                                        layer))
@@ -68,6 +68,14 @@ def run_prefill(cuda, B, T, hidden, H, Hkv, layer, seed, rows=None):
 @pytest.mark.parametrize("B,T,hidden,H,Hkv", [(2, 300, 512, 4, 1), (1, 129, 264, 8, 2)])
 def test_layer_prefill_small(cuda, layer, B, T, hidden, H, Hkv):
     run_prefill(cuda, B, T, hidden, H, Hkv, layer, seed=31)
+
+
+@pytest.mark.parametrize("kind", [FULL, SLIDING], ids=["full", "sliding"])
+def test_layer_prefill_silu_gate(cuda, kind):
+    # gate_attn_act_mode = silu (Spark §3); logits kept O(1) so that the
+    # gate's factor (up to |g|) does not scale the bf16 rounding past the bar
+    layer = wl.Layer(kind=kind, window=64, theta=1e4, rot_dim=256, gate_mode=1)
+    run_prefill(cuda, 2, 150, 512, 4, 1, layer, seed=44, gate_scale=0.3)
 
 
 def test_layer_prefill_1p7b_sliding_whole(cuda):
@@ -127,7 +135,8 @@ def test_layer_prefill_fills_the_cache(cuda):
 @pytest.mark.parametrize("layer,cap,positions", [
     (wl.FULL_LAYER, 5000, [0, 17, 4095, 4999]),
     (wl.SLIDING_LAYER, 512, [0, 511, 512, 70000]),
-], ids=["full", "sliding"])
+    (wl.SLIDING_LAYER, 512, [1, 3, 100, 300]),
+], ids=["full", "sliding", "sliding-ring-filling"])
 def test_layer_decode_4b(cuda, layer, cap, positions):
     B, hidden, H, Hkv = len(positions), 2560, 16, 4
     x = hidden_states((B, hidden), 38)

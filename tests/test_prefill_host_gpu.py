@@ -33,6 +33,17 @@ def test_host_prefill_equals_device_prefill(cuda, layer, B, T, pinned):
     assert torch.equal(got, want.cpu())
 
 
+def test_host_prefill_silu_gate(cuda):
+    layer = wl.Layer(kind=wl.SLIDING, window=100, theta=1e4, rot_dim=256, gate_mode=1)
+    case = wl.PrefillCase("h", B=3, T=160, H=16, Hkv=4, layer=layer, seed=62)
+    x = wl.make_prefill_inputs(case)
+    want = fga.spark_attn_prefill(x["qkv"].to(cuda), x["gate"].to(cuda), x["pos"].to(cuda), layer)
+    got = fga.spark_attn_prefill_host(x["qkv"].pin_memory(), x["gate"].pin_memory(),
+                                      x["pos"].pin_memory(), layer)
+    torch.cuda.synchronize()
+    assert torch.equal(got, want.cpu())
+
+
 def test_host_prefill_matches_the_oracle(cuda):
     case = wl.PrefillCase("h", B=2, T=200, H=8, Hkv=2, layer=wl.SLIDING_LAYER, seed=61)
     x = wl.make_prefill_inputs(case)
