@@ -8,8 +8,9 @@ One step is one pass of the whole hot path over one batch of synthetic input:
     layers with full 512-slot rings): 38.71 GB of KV read.
 The JSON line's value is the prefill throughput (TFLOP/s); the decode KV-read
 bandwidth is reported beside it.  Outside the timed step the line also carries
-the 1.7B sliding prefill (B=1, T=1024) per call and in a CUDA graph, and the
-whole attention block of the prefill layer (projections + core).  Inputs are seeded synthetic tensors of the
+the 1.7B sliding prefill (B=1, T=1024) per call and in a CUDA graph, the whole
+attention block of the prefill layer (projections + core), and the decode step
+through all 36 attention blocks.  Inputs are seeded synthetic tensors of the
 model's shapes (no dataset or weights exist for this path).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {ours,reference}]
@@ -432,6 +433,8 @@ def run_ours(args, rank, world, local):
     if pre is not None and rank == 0:
         line["small_prefill"] = time_small_prefill(fga, dev, bf16_peak)
         line["layer_prefill"] = time_layer_prefill(fga, dev, bf16_peak)
+    if dec and rank == 0:
+        line["layer_decode"] = time_layer_decode(fga, dev, dec, hbm_peak)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args)
     return line
@@ -540,6 +543,64 @@ def time_layer_prefill(fga, dev, bf16_peak, calls=10):
         "tflops": flops / ms / 1e9, "frac_bf16_peak": flops / ms / 1e9 / bf16_peak,
         "calls": calls, "projections": "cuBLASLt bf16 GEMMs, fp32 accumulation",
         "device_status": fga.spark_attn_read_status(ws),
+    }
+
+
+def time_layer_decode(fga, dev, dec, hbm_peak, steps=5):
+    """One decode step through all the attention blocks of the decode
+    workload (the 36 layers of the 4B model at 1M context): per layer
+    q_k_v_proj and g_proj of one hidden state (cuBLASLt), the core on that
+    layer's cache, out_proj.  Seeded random weights of the model's shapes
+    (1.9 GB for 36 layers).  Bytes = the core's KV read plus the projection
+    weights, the two streams a decode step must read."""
+    import torch
+    hidden = 2560
+    g = torch.Generator().manual_seed(12)
+    blocks = []
+    for L in dec:
+        c = L["case"]
+        width = (c.H + 2 * c.Hkv) * 256
+        w_qkv = (torch.randn((width, hidden), generator=g) / hidden ** 0.5).to(torch.bfloat16)
+        w_g = (torch.randn((c.H, hidden), generator=g) / hidden ** 0.5).to(torch.bfloat16)
+        w_o = (torch.randn((hidden, c.H * 256), generator=g) / (c.H * 256) ** 0.5).to(
+            torch.bfloat16)
+        x = torch.randn((c.B, hidden), generator=g).to(torch.bfloat16)
+        blocks.append({
+            "w": [w_qkv.to(dev), w_g.to(dev), w_o.to(dev)], "x": x.to(dev),
+            "y": torch.empty((c.B, hidden), dtype=torch.bfloat16, device=dev),
+            "ws": fga.new_workspace(fga.spark_attn_layer_decode_workspace_size(
+                c.B, hidden, c.H, c.Hkv, c.cap, L["layer"]), dev),
+        })
+    stream = torch.cuda.current_stream()
+
+    def one_step():
+        for L, bl in zip(dec, blocks):
+            fga.spark_attn_layer_decode(bl["x"], *bl["w"], L["dev"]["pos"], L["k"], L["v"],
+                                        L["layer"], y=bl["y"], workspace=bl["ws"], stream=stream)
+
+    for _ in range(3):
+        one_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    kv, _ = decode_kv_bytes([L["layer"] for L in dec])
+    weights = sum(sum(w.numel() * w.element_size() for w in bl["w"]) for bl in blocks)
+    status = 0
+    for bl in blocks:
+        status |= fga.spark_attn_read_status(bl["ws"])
+    gbs = (kv + weights) / ms / 1e6
+    return {
+        "workload": f"1M-context decode step through all {len(dec)} attention blocks "
+                    "(q_k_v_proj + g_proj, core, out_proj; random weights), B=1",
+        "ms": ms, "kv_bytes": kv, "weight_bytes": weights, "gbs": gbs,
+        "frac_hbm_peak": gbs / hbm_peak, "steps": steps,
+        "projections": "cuBLASLt bf16 GEMMs (M = 1), fp32 accumulation",
+        "device_status": status,
     }
 
 
