@@ -7,11 +7,13 @@
 // (H * 256 -> hidden) maps the gated attention output back.  §1: the
 // checkpoints run in bfloat16 and the pages list no biases.
 //
-// The three projections are plain dense GEMMs and run through cuBLASLt (bf16
-// operands, fp32 accumulation) on the caller's stream, with the caller's
-// workspace as cuBLASLt's scratch.  The gate GEMM accumulates in fp32 and a
-// small kernel rounds its result to bf16, the dtype of the Linear's output,
-// before the core's epilogue takes sigmoid of it in fp32.
+// With more than a few rows the three projections are plain dense GEMMs and
+// run through cuBLASLt (bf16 operands, fp32 accumulation) on the caller's
+// stream, with the caller's workspace as cuBLASLt's scratch; the gate GEMM
+// accumulates in fp32 and a small kernel rounds its result to bf16, the dtype
+// of the Linear's output, before the core's epilogue takes sigmoid of it in
+// fp32.  With at most kGemvMaxM rows (a decode step) they are weight-streaming
+// GEMVs of this file, g_proj in the same pass as q_k_v_proj.
 #include <cublasLt.h>
 
 #include <map>
@@ -44,6 +46,100 @@ __global__ void round_gate_kernel(float *g, long long n) {
     grid_dep_launch();
     const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i < n) g[i] = __bfloat162float(__float2bfloat16_rn(g[i]));
+}
+
+// ---------------------------------------------------------------- decode GEMV
+//
+// A decode step projects one hidden state per sequence: y = W x for a few
+// vectors x, which reads the whole weight matrix once and is bound by that
+// read.  Each warp takes kGemvRows weight rows and streams them with 16-byte
+// loads (the few x vectors come from L1), accumulates in fp32, reduces over
+// the warp and rounds once to bf16.  One launch can cover two matrices (the
+// rows of W_qkv, then those of W_g), so g_proj rides along with q_k_v_proj.
+
+constexpr int kGemvRows = 2;      // weight rows per warp
+constexpr int kGemvWarps = 8;     // warps per CTA
+constexpr int kGemvMaxM = 8;      // vectors per launch
+
+struct GemvSeg {
+    const __nv_bfloat16 *w;       // [n][K] row-major
+    void *out;                    // [M][n]: bf16, or fp32 holding bf16-rounded values
+    int n;                        // rows
+    int out_f32;                  // output type
+};
+
+__global__ void __launch_bounds__(kGemvWarps * 32) gemv_kernel(GemvSeg s0, GemvSeg s1,
+                                                               const __nv_bfloat16 *x, int M,
+                                                               int K) {
+    grid_dep_wait();  // x may come from the previous kernel
+    grid_dep_launch();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row0 = (blockIdx.x * kGemvWarps + warp) * kGemvRows;
+    float acc[kGemvRows][kGemvMaxM];
+#pragma unroll
+    for (int r = 0; r < kGemvRows; ++r)
+#pragma unroll
+        for (int m = 0; m < kGemvMaxM; ++m) acc[r][m] = 0.f;
+    const __nv_bfloat16 *wrow[kGemvRows];
+#pragma unroll
+    for (int r = 0; r < kGemvRows; ++r) {
+        const int n = row0 + r;
+        wrow[r] = (n < s0.n) ? s0.w + static_cast<size_t>(n) * K
+                  : (n < s0.n + s1.n) ? s1.w + static_cast<size_t>(n - s0.n) * K : nullptr;
+    }
+#pragma unroll 4
+    for (int k = lane * 8; k < K; k += 32 * 8) {
+        uint4 wv[kGemvRows];
+#pragma unroll
+        for (int r = 0; r < kGemvRows; ++r)
+            wv[r] = wrow[r] ? __ldcs(reinterpret_cast<const uint4 *>(wrow[r] + k))
+                            : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int m = 0; m < kGemvMaxM; ++m) {
+            if (m >= M) break;
+            const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(x + static_cast<size_t>(m) * K + k));
+            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+            for (int r = 0; r < kGemvRows; ++r) {
+                const uint32_t ww[4] = {wv[r].x, wv[r].y, wv[r].z, wv[r].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[r][m] = fmaf(bf16_lo(ww[i]), bf16_lo(xw[i]), acc[r][m]);
+                    acc[r][m] = fmaf(bf16_hi(ww[i]), bf16_hi(xw[i]), acc[r][m]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < kGemvRows; ++r) {
+#pragma unroll
+        for (int m = 0; m < kGemvMaxM; ++m) {
+            if (m >= M) break;
+            float v = acc[r][m];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+            const int n = row0 + r;
+            if (lane == 0 && wrow[r]) {
+                const GemvSeg &sg = (n < s0.n) ? s0 : s1;
+                const int nn = (n < s0.n) ? n : n - s0.n;
+                const __nv_bfloat16 b = __float2bfloat16_rn(v);
+                if (sg.out_f32)
+                    static_cast<float *>(sg.out)[static_cast<size_t>(m) * sg.n + nn] =
+                        __bfloat162float(b);
+                else
+                    static_cast<__nv_bfloat16 *>(sg.out)[static_cast<size_t>(m) * sg.n + nn] = b;
+            }
+        }
+    }
+}
+
+cudaError_t launch_gemv(const GemvSeg &s0, const GemvSeg &s1, const void *x, int M, int K,
+                        cudaStream_t stream) {
+    const long long rows = static_cast<long long>(s0.n) + s1.n;
+    const long long warps = (rows + kGemvRows - 1) / kGemvRows;
+    const unsigned grid = static_cast<unsigned>((warps + kGemvWarps - 1) / kGemvWarps);
+    return launch_overlapped(gemv_kernel, dim3(grid), dim3(kGemvWarps * 32), 0, stream, s0, s1,
+                             static_cast<const __nv_bfloat16 *>(x), M, K);
 }
 
 std::mutex g_lt_mu;
@@ -187,6 +283,14 @@ spark_status project_in(cublasLtHandle_t h, const void *x, const void *w_qkv, co
                         long long rows, int hidden, int H, int Hkv, uint8_t *ws,
                         const LayerPlan &pl, cudaStream_t stream) {
     const int M = static_cast<int>(rows);
+    if (M <= kGemvMaxM) {
+        // a few hidden states: one weight-streaming pass over W_qkv and W_g
+        const GemvSeg qkv{static_cast<const __nv_bfloat16 *>(w_qkv), ws + pl.qkv,
+                          (H + 2 * Hkv) * kHeadDim, 0};
+        const GemvSeg gate{static_cast<const __nv_bfloat16 *>(w_g), ws + pl.gate, H, 1};
+        return launch_gemv(qkv, gate, x, M, hidden, stream) == cudaSuccess ? SPARK_OK
+                                                                           : SPARK_ERR_CUDA;
+    }
     if (!linear(h, x, w_qkv, ws + pl.qkv, CUDA_R_16BF, M, (H + 2 * Hkv) * kHeadDim, hidden,
                 ws + pl.lt, stream) ||
         !linear(h, x, w_g, ws + pl.gate, CUDA_R_32F, M, H, hidden, ws + pl.lt, stream))
@@ -196,6 +300,23 @@ spark_status project_in(cublasLtHandle_t h, const void *x, const void *w_qkv, co
                                             dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256),
                                             0, stream, reinterpret_cast<float *>(ws + pl.gate), n);
     return e == cudaSuccess ? SPARK_OK : SPARK_ERR_CUDA;
+}
+
+// out_proj of `rows` gated attention outputs: y = a W_o^T.
+spark_status project_out(cublasLtHandle_t h, const void *attn, const void *w_o, void *y,
+                         long long rows, int hidden, int H, uint8_t *ws, const LayerPlan &pl,
+                         cudaStream_t stream) {
+    const int M = static_cast<int>(rows);
+    if (M <= kGemvMaxM) {
+        const GemvSeg out{static_cast<const __nv_bfloat16 *>(w_o), y, hidden, 0};
+        const GemvSeg none{nullptr, nullptr, 0, 0};
+        return launch_gemv(out, none, attn, M, H * kHeadDim, stream) == cudaSuccess
+                   ? SPARK_OK
+                   : SPARK_ERR_CUDA;
+    }
+    return linear(h, attn, w_o, y, CUDA_R_16BF, M, hidden, H * kHeadDim, ws + pl.lt, stream)
+               ? SPARK_OK
+               : SPARK_ERR_CUDA;
 }
 
 }  // namespace
@@ -253,10 +374,7 @@ spark_status spark_attn_layer_prefill(const void *x, const void *w_qkv, const vo
     st = prefill_impl(qkv, gate, pos, desc, B, T, H, Hkv, attn, k_cache, v_cache, cap, nullptr,
                       ws, core, stream, false);
     if (st != SPARK_OK) return st;
-    return linear(h, attn, w_o, y, CUDA_R_16BF, static_cast<int>(rows), hidden, H * kHeadDim,
-                  ws + pl.lt, s)
-               ? SPARK_OK
-               : SPARK_ERR_CUDA;
+    return project_out(h, attn, w_o, y, rows, hidden, H, ws, pl, s);
 }
 
 size_t spark_attn_layer_decode_workspace_size(int B, int hidden, int H, int Hkv, int64_t cap,
@@ -304,9 +422,7 @@ spark_status spark_attn_layer_decode(const void *x, const void *w_qkv, const voi
     st = decode_impl(qkv, gate, pos, k_cache, v_cache, cap, desc, B, H, Hkv, attn, ws, core,
                      stream, false);
     if (st != SPARK_OK) return st;
-    return linear(h, attn, w_o, y, CUDA_R_16BF, B, hidden, H * kHeadDim, ws + pl.lt, s)
-               ? SPARK_OK
-               : SPARK_ERR_CUDA;
+    return project_out(h, attn, w_o, y, B, hidden, H, ws, pl, s);
 }
 
 }  // extern "C"

@@ -162,6 +162,29 @@ def test_layer_decode_4b(cuda, layer, cap, positions):
         assert np.all(np.abs(vb[b, :, slot] - v_new[b]) <= 2.0 ** -7 * np.abs(v_new[b]) + 2.0 ** -12)
 
 
+@pytest.mark.parametrize("B", [1, 8, 12], ids=["gemv-1", "gemv-8", "gemm-12"])
+def test_layer_decode_batch_sizes(cuda, B):
+    # up to 8 sequences the projections are the library's weight-streaming
+    # GEMV (g_proj fused with q_k_v_proj); beyond, cuBLASLt GEMMs
+    layer, cap, hidden, H, Hkv = wl.SLIDING_LAYER, 512, 2560, 16, 4
+    x = hidden_states((B, hidden), 45)
+    w = weights(hidden, H, Hkv, 46)
+    kc = wl.fill_cache_(torch.empty((B, Hkv, cap, D), dtype=torch.bfloat16), 47)
+    vc = wl.fill_cache_(torch.empty_like(kc), 48)
+    pos = torch.tensor([(97 * b + 5) % 3000 for b in range(B)], dtype=torch.int32)
+    y = fga.spark_attn_layer_decode(x.to(cuda), *[t.to(cuda) for t in w], pos.to(cuda),
+                                    kc.to(cuda), vc.to(cuda), layer)
+    want, _, _ = oracle.layer_decode(bits(x), *[bits(t) for t in w], pos.numpy(), bits(kc),
+                                     bits(vc), layer.kind, layer.window, layer.theta,
+                                     layer.rot_dim, H, Hkv)
+    check_close(y, want, f"layer decode B={B}")
+
+
+def test_layer_prefill_few_rows_uses_gemv(cuda):
+    # B*T <= 8 rows: the projections take the GEMV path in prefill too
+    run_prefill(cuda, 2, 3, 512, 4, 1, wl.FULL_LAYER, seed=49)
+
+
 def test_layer_rejects_before_enqueueing(cuda):
     """A cache too small for the core is refused before the projections run."""
     B, T, hidden, H, Hkv = 1, 64, 512, 4, 1
