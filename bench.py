@@ -37,6 +37,9 @@ if ROOT not in sys.path:
 import workloads as wl  # noqa: E402
 
 PREFILL = wl.PREFILL_FULL_4B_B2_T8192
+# the same shapes as a sliding_attention layer, for profiling (--prefill-layer sliding)
+PREFILL_SLIDING_B2_T8192 = wl.scaled(wl.PREFILL_FULL_4B_B2_T8192,
+                                     name="prefill_sliding_4b_B2_T8192", layer=wl.SLIDING_LAYER)
 DECODE_FULL = wl.DECODE_FULL_4B_1M
 DECODE_SLIDING = wl.DECODE_SLIDING_4B_1M
 METRIC = "prefill attn TFLOP/s & % bf16 peak; decode KV-read GB/s & % HBM peak (1 GB300)"
@@ -400,11 +403,16 @@ def run_ours(args, rank, world, local):
         "dtype": "bf16",
         "data": "synthetic (seeded normal activations and KV caches at the 4B model shapes)",
         "config": {
-            "workload": ("prefill 4B full_attention B=2 T=8192 H=16 Hkv=4 + 1M-context "
+            "workload": (f"prefill 4B {'full' if PREFILL.layer.kind == wl.FULL else 'sliding'}"
+                         "_attention B=2 T=8192 H=16 Hkv=4 + 1M-context "
                          "36-layer 4B decode step (9 full, 27 sliding)"
                          if (pre is not None and dec) else args.only),
             "prefill": {"B": PREFILL.B, "T": PREFILL.T, "H": PREFILL.H, "Hkv": PREFILL.Hkv,
-                        "kind": "full", "rope_theta": 5e6, "rot_dim": 64} if pre else None,
+                        "kind": "full" if PREFILL.layer.kind == wl.FULL else "sliding",
+                        "window": PREFILL.layer.window if PREFILL.layer.kind == wl.SLIDING
+                        else None,
+                        "rope_theta": PREFILL.layer.theta, "rot_dim": PREFILL.layer.rot_dim}
+            if pre else None,
             "decode": {"B": 1, "layers": len(dec), "full_layers": n_full,
                        "cached_tokens": DECODE_FULL.len_hi, "ring_slots": 512} if dec else None,
             "parallelism": f"replicas x{world}",
@@ -588,6 +596,26 @@ def time_layer_decode(fga, dev, dec, hbm_peak, steps=5):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
+    # the same step captured in a CUDA graph, as a serving loop would replay it
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph):
+            cap_stream = torch.cuda.current_stream()
+            for L, bl in zip(dec, blocks):
+                fga.spark_attn_layer_decode(bl["x"], *bl["w"], L["dev"]["pos"], L["k"], L["v"],
+                                            L["layer"], y=bl["y"], workspace=bl["ws"],
+                                            stream=cap_stream)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = e0.elapsed_time(e1) / steps
     kv, _ = decode_kv_bytes([L["layer"] for L in dec])
     weights = sum(sum(w.numel() * w.element_size() for w in bl["w"]) for bl in blocks)
     status = 0
@@ -599,6 +627,7 @@ def time_layer_decode(fga, dev, dec, hbm_peak, steps=5):
                     "(q_k_v_proj + g_proj, core, out_proj; random weights), B=1",
         "ms": ms, "kv_bytes": kv, "weight_bytes": weights, "gbs": gbs,
         "frac_hbm_peak": gbs / hbm_peak, "steps": steps,
+        "graph_ms": graph_ms, "graph_gbs": (kv + weights) / graph_ms / 1e6,
         "projections": "cuBLASLt bf16 GEMMs (M = 1), fp32 accumulation",
         "device_status": status,
     }
@@ -711,10 +740,16 @@ def main(argv=None):
                     help="cached tokens of each full decode layer (default 1,048,575); "
                          "smaller values are for profiler captures")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill-layer", choices=("full", "sliding"), default="full",
+                    help="layer type of the prefill workload (sliding: for profiling; the "
+                         "benchmark's workload is the full layer)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         print("bench.py: warmup raised to 3", file=sys.stderr)
         args.warmup = 3
+    if args.prefill_layer == "sliding":
+        global PREFILL
+        PREFILL = PREFILL_SLIDING_B2_T8192
     if args.decode_cache_tokens is not None:
         global DECODE_FULL
         n = args.decode_cache_tokens

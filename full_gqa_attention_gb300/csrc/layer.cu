@@ -52,13 +52,14 @@ __global__ void round_gate_kernel(float *g, long long n) {
 //
 // A decode step projects one hidden state per sequence: y = W x for a few
 // vectors x, which reads the whole weight matrix once and is bound by that
-// read.  Each warp takes kGemvRows weight rows and streams them with 16-byte
-// loads (the few x vectors come from L1), accumulates in fp32, reduces over
+// read.  Each warp takes one weight row and streams it in blocks of
+// kGemvBlk coalesced 16-byte loads per lane, all issued before any of them is
+// used (the few x vectors come from L1), accumulates in fp32, reduces over
 // the warp and rounds once to bf16.  One launch can cover two matrices (the
 // rows of W_qkv, then those of W_g), so g_proj rides along with q_k_v_proj.
 
-constexpr int kGemvRows = 2;      // weight rows per warp
-constexpr int kGemvWarps = 8;     // warps per CTA
+constexpr int kGemvWarps = 8;     // warps (rows) per CTA
+constexpr int kGemvBlk = 8;       // 16-byte loads in flight per lane
 constexpr int kGemvMaxM = 8;      // vectors per launch
 
 struct GemvSeg {
@@ -74,61 +75,53 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_kernel(GemvSeg s0, GemvS
     grid_dep_wait();  // x may come from the previous kernel
     grid_dep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row0 = (blockIdx.x * kGemvWarps + warp) * kGemvRows;
-    float acc[kGemvRows][kGemvMaxM];
+    const int n = blockIdx.x * kGemvWarps + warp;
+    if (n >= s0.n + s1.n) return;
+    const bool first = n < s0.n;
+    const GemvSeg &sg = first ? s0 : s1;
+    const int nn = first ? n : n - s0.n;
+    const __nv_bfloat16 *w = sg.w + static_cast<size_t>(nn) * K;
+    float acc[kGemvMaxM];
 #pragma unroll
-    for (int r = 0; r < kGemvRows; ++r)
+    for (int m = 0; m < kGemvMaxM; ++m) acc[m] = 0.f;
+    for (int kb = 0; kb < K; kb += 32 * 8 * kGemvBlk) {
+        uint4 wv[kGemvBlk];
 #pragma unroll
-        for (int m = 0; m < kGemvMaxM; ++m) acc[r][m] = 0.f;
-    const __nv_bfloat16 *wrow[kGemvRows];
+        for (int c = 0; c < kGemvBlk; ++c) {
+            const int k = kb + (c * 32 + lane) * 8;
+            wv[c] = (k < K) ? __ldcs(reinterpret_cast<const uint4 *>(w + k)) : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
-    for (int r = 0; r < kGemvRows; ++r) {
-        const int n = row0 + r;
-        wrow[r] = (n < s0.n) ? s0.w + static_cast<size_t>(n) * K
-                  : (n < s0.n + s1.n) ? s1.w + static_cast<size_t>(n - s0.n) * K : nullptr;
-    }
-#pragma unroll 4
-    for (int k = lane * 8; k < K; k += 32 * 8) {
-        uint4 wv[kGemvRows];
+        for (int c = 0; c < kGemvBlk; ++c) {
+            const int k = kb + (c * 32 + lane) * 8;
+            if (k >= K) break;
+            const uint32_t ww[4] = {wv[c].x, wv[c].y, wv[c].z, wv[c].w};
 #pragma unroll
-        for (int r = 0; r < kGemvRows; ++r)
-            wv[r] = wrow[r] ? __ldcs(reinterpret_cast<const uint4 *>(wrow[r] + k))
-                            : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int m = 0; m < kGemvMaxM; ++m) {
-            if (m >= M) break;
-            const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(x + static_cast<size_t>(m) * K + k));
-            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-            for (int r = 0; r < kGemvRows; ++r) {
-                const uint32_t ww[4] = {wv[r].x, wv[r].y, wv[r].z, wv[r].w};
+            for (int m = 0; m < kGemvMaxM; ++m) {
+                if (m >= M) break;
+                const uint4 xv =
+                    __ldg(reinterpret_cast<const uint4 *>(x + static_cast<size_t>(m) * K + k));
+                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    acc[r][m] = fmaf(bf16_lo(ww[i]), bf16_lo(xw[i]), acc[r][m]);
-                    acc[r][m] = fmaf(bf16_hi(ww[i]), bf16_hi(xw[i]), acc[r][m]);
+                    acc[m] = fmaf(bf16_lo(ww[i]), bf16_lo(xw[i]), acc[m]);
+                    acc[m] = fmaf(bf16_hi(ww[i]), bf16_hi(xw[i]), acc[m]);
                 }
             }
         }
     }
 #pragma unroll
-    for (int r = 0; r < kGemvRows; ++r) {
+    for (int m = 0; m < kGemvMaxM; ++m) {
+        if (m >= M) break;
+        float v = acc[m];
 #pragma unroll
-        for (int m = 0; m < kGemvMaxM; ++m) {
-            if (m >= M) break;
-            float v = acc[r][m];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-            const int n = row0 + r;
-            if (lane == 0 && wrow[r]) {
-                const GemvSeg &sg = (n < s0.n) ? s0 : s1;
-                const int nn = (n < s0.n) ? n : n - s0.n;
-                const __nv_bfloat16 b = __float2bfloat16_rn(v);
-                if (sg.out_f32)
-                    static_cast<float *>(sg.out)[static_cast<size_t>(m) * sg.n + nn] =
-                        __bfloat162float(b);
-                else
-                    static_cast<__nv_bfloat16 *>(sg.out)[static_cast<size_t>(m) * sg.n + nn] = b;
-            }
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (lane == 0) {
+            const __nv_bfloat16 b = __float2bfloat16_rn(v);
+            if (sg.out_f32)
+                static_cast<float *>(sg.out)[static_cast<size_t>(m) * sg.n + nn] = __bfloat162float(b);
+            else
+                static_cast<__nv_bfloat16 *>(sg.out)[static_cast<size_t>(m) * sg.n + nn] = b;
         }
     }
 }
@@ -136,8 +129,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_kernel(GemvSeg s0, GemvS
 cudaError_t launch_gemv(const GemvSeg &s0, const GemvSeg &s1, const void *x, int M, int K,
                         cudaStream_t stream) {
     const long long rows = static_cast<long long>(s0.n) + s1.n;
-    const long long warps = (rows + kGemvRows - 1) / kGemvRows;
-    const unsigned grid = static_cast<unsigned>((warps + kGemvWarps - 1) / kGemvWarps);
+    const unsigned grid = static_cast<unsigned>((rows + kGemvWarps - 1) / kGemvWarps);
     return launch_overlapped(gemv_kernel, dim3(grid), dim3(kGemvWarps * 32), 0, stream, s0, s1,
                              static_cast<const __nv_bfloat16 *>(x), M, K);
 }
