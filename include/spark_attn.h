@@ -135,10 +135,11 @@ spark_status spark_attn_prefill(const void *qkv, const float *gate, const int32_
  *              256-byte aligned, zeroed once before first use (its status word
  *              is read with spark_attn_read_status)
  *
- * The batch goes through two device staging areas one sequence at a time:
- * the copy-in of sequence b+1 and the copy-out of sequence b-1 run on two
- * copy streams that the library creates per device on first use, while
- * `stream` computes sequence b.  Host buffers should be pinned
+ * The batch goes through device staging areas one piece at a time -- a
+ * sequence, or a chunk of 2048 tokens of a longer one (processed as a chunked
+ * prefill over a device KV cache in the workspace): copy-ins of later pieces
+ * and copy-outs of earlier ones run on two copy streams that the library
+ * creates per device on first use, while `stream` computes.  Host buffers should be pinned
  * (cudaHostAlloc / cudaHostRegister); pageable memory still works, with
  * copies that do not overlap.  The call returns once everything is enqueued:
  * synchronize `stream` before reading out_h (work enqueued on `stream` after

@@ -65,3 +65,38 @@ def test_host_prefill_empty_and_rejects(cuda):
     with pytest.raises(TypeError):
         fga.spark_attn_prefill_host(e.to(cuda), torch.empty((0, 4, 16)),
                                     torch.empty((0, 4), dtype=torch.int32), layer)
+
+
+def test_host_prefill_long_sequences_full_layer_bit_exact(cuda):
+    """Sequences longer than one host chunk (2048 tokens) go through in chunks
+    over a device KV cache; on a full layer the chunks' query and key tiles
+    fall where the one-shot prefill puts them, so the output is identical."""
+    case = wl.PrefillCase("hl", B=2, T=4500, H=16, Hkv=4, layer=wl.FULL_LAYER, seed=63)
+    x = wl.make_prefill_inputs(case)
+    want = fga.spark_attn_prefill(x["qkv"].to(cuda), x["gate"].to(cuda), x["pos"].to(cuda),
+                                  case.layer)
+    ws = fga.new_workspace(fga.spark_attn_prefill_host_workspace_size(2, 4500, 16, 4, case.layer))
+    got = fga.spark_attn_prefill_host(x["qkv"].pin_memory(), x["gate"].pin_memory(),
+                                      x["pos"].pin_memory(), case.layer, workspace=ws)
+    torch.cuda.synchronize()
+    assert fga.spark_attn_read_status(ws) == 0
+    assert torch.equal(got, want.cpu())
+
+
+def test_host_prefill_long_sequences_sliding_layer(cuda):
+    """On a sliding layer the chunks read a ring in 128-aligned key tiles, so
+    the rounding order differs from the one-shot prefill: checked against the
+    oracle on rows around every chunk edge and the window edge."""
+    case = wl.PrefillCase("hs", B=2, T=4500, H=16, Hkv=4, layer=wl.SLIDING_LAYER, seed=64)
+    x = wl.make_prefill_inputs(case)
+    got = fga.spark_attn_prefill_host(x["qkv"].pin_memory(), x["gate"].pin_memory(),
+                                      x["pos"].pin_memory(), case.layer)
+    torch.cuda.synchronize()
+    import numpy as np
+    edges = [0, 511, 512, 2047, 2048, 2049, 2559, 2560, 4095, 4096, 4499]
+    rows = np.array(sorted({b * 4500 + t for b in (0, 1) for e in edges
+                            for t in range(max(0, e - 2), min(4500, e + 3))}))
+    L = case.layer
+    want = oracle.prefill(wl.bf16_bits(x["qkv"]), x["gate"].numpy(), x["pos"].numpy(), L.kind,
+                          L.window, L.theta, L.rot_dim, 16, 4, rows=rows)
+    check_close(got.reshape(9000, -1)[torch.as_tensor(rows)], want, "host prefill sliding chunks")
