@@ -443,6 +443,8 @@ def run_ours(args, rank, world, local):
         line["layer_prefill"] = time_layer_prefill(fga, dev, bf16_peak)
     if dec and rank == 0:
         line["layer_decode"] = time_layer_decode(fga, dev, dec, hbm_peak)
+    if pre is not None and dec and rank == 0 and not args.no_other_configs:
+        line["other_configs"] = time_other_configs(fga, dev, bf16_peak, hbm_peak)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args)
     return line
@@ -633,6 +635,71 @@ def time_layer_decode(fga, dev, dec, hbm_peak, steps=5):
     }
 
 
+def time_other_configs(fga, dev, bf16_peak, hbm_peak):
+    """The remaining workloads of the benchmark's configuration list, each
+    timed on its own (CUDA events, inputs resident): the long 4B prefill
+    (B=1, T=65536) as a full and as a sliding layer, and the batched 4B decode
+    (B=64, per-sequence lengths 4096..131072) on a full layer and on
+    512-slot rings.  Not part of the timed step."""
+    import torch
+    out = {}
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, calls):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(calls):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / calls
+
+    for key, c, calls in (("long_prefill_full", wl.PREFILL_FULL_4B_T65536, 3),
+                          ("long_prefill_sliding", wl.PREFILL_SLIDING_4B_T65536, 10)):
+        x = wl.make_prefill_inputs(c)
+        q, g, p = (x[k].to(dev) for k in ("qkv", "gate", "pos"))
+        o = torch.empty((c.B, c.T, c.H * 256), dtype=torch.bfloat16, device=dev)
+        ws = fga.new_workspace(fga.spark_attn_prefill_workspace_size(c.B, c.T, c.H, c.Hkv,
+                                                                     c.layer), dev)
+        ms = timed(lambda: fga.spark_attn_prefill(q, g, p, c.layer, out=o, workspace=ws,
+                                                  stream=stream), calls)
+        flops = prefill_flops(c)
+        out[key] = {"workload": f"{c.name}: B={c.B} T={c.T} H={c.H} Hkv={c.Hkv}", "ms": ms,
+                    "tflops": flops / ms / 1e9, "frac_bf16_peak": flops / ms / 1e9 / bf16_peak,
+                    "device_status": fga.spark_attn_read_status(ws)}
+        del q, g, p, o, ws, x
+        torch.cuda.empty_cache()
+    for key, c in (("batched_decode_full", wl.DECODE_FULL_4B_B64),
+                   ("batched_decode_sliding", wl.DECODE_SLIDING_4B_B64)):
+        step = wl.make_decode_step_inputs(c)
+        k = torch.empty((c.B, c.Hkv, c.cap, 256), dtype=torch.bfloat16, device=dev)
+        v = torch.empty_like(k)
+        gen = torch.Generator(dev).manual_seed(c.seed)
+        k.normal_(generator=gen)
+        v.normal_(generator=gen)
+        q, g, p = (step[n].to(dev) for n in ("qkv", "gate", "pos"))
+        o = torch.empty((c.B, c.H * 256), dtype=torch.bfloat16, device=dev)
+        ws = fga.new_workspace(fga.spark_attn_decode_workspace_size(c.B, c.H, c.Hkv, c.cap,
+                                                                    c.layer), dev)
+        ms = timed(lambda: fga.spark_attn_decode(q, g, p, k, v, c.layer, out=o, workspace=ws,
+                                                 stream=stream), 10)
+        # visible tokens per sequence, the new one included (as for the step's decode)
+        lens = step["pos"].long() + 1
+        visible = lens if c.layer.kind == wl.FULL else lens.clamp(max=c.layer.window)
+        kv = int(visible.sum()) * KV_BYTES_PER_TOKEN
+        gbs = kv / ms / 1e6
+        out[key] = {"workload": f"{c.name}: B={c.B}, lengths {c.len_lo}..{c.len_hi}, "
+                                f"cache slots {c.cap}", "ms": ms, "kv_bytes": kv, "kv_gbs": gbs,
+                    "frac_hbm_peak": gbs / hbm_peak,
+                    "device_status": fga.spark_attn_read_status(ws)}
+        del k, v, q, g, p, o, ws
+        torch.cuda.empty_cache()
+    return out
+
+
 # Per-launch DRAM traffic (read + write bytes) from ncu captures of the
 # current kernels, scaled to one launch of the bench workload; None when the
 # kernels changed since the counters were taken.
@@ -740,6 +807,8 @@ def main(argv=None):
                     help="cached tokens of each full decode layer (default 1,048,575); "
                          "smaller values are for profiler captures")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="skip the extra lines for the long prefill and the batched decode")
     ap.add_argument("--prefill-layer", choices=("full", "sliding"), default="full",
                     help="layer type of the prefill workload (sliding: for profiling; the "
                          "benchmark's workload is the full layer)")
