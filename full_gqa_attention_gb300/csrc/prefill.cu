@@ -262,10 +262,24 @@ __device__ __forceinline__ void named_bar(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-// kFromCache: chunked prefill.  Queries are chunk tokens at absolute index
-// start[b] + t, keys are read from the KV cache (which already holds this
-// chunk's keys and values) and tm_kv_k / tm_kv_v then map the caches.
-template <bool kFromCache>
+// Where the keys and values come from: the fused projection (one-shot
+// prefill), or the KV cache of a chunked prefill -- a full layer's, one slot
+// per token, or a sliding layer's ring.  In a chunked prefill the queries are
+// chunk tokens at absolute index start[b] + t, the cache already holds this
+// chunk's keys and values, and tm_kv_k / tm_kv_v map the caches.  Each source
+// is its own instantiation, so that no kernel carries another's addressing
+// (the ring's slot arithmetic would sit in every inlined load of the
+// producer).
+enum KvSource : int { kKvFromQkv = 0, kKvFromCache = 1, kKvFromRing = 2 };
+
+// The layer kind is a template argument too, so that a kernel carries no
+// arithmetic of the other kind; kKindAny reads it from P.kind instead.  Which
+// instantiation serves which layer was chosen by timing: the kind-specialised
+// builds are faster for both chunked kinds and the one-shot sliding layer,
+// the generic one for the one-shot full layer.
+constexpr int kKindAny = -1;
+
+template <int kSrc, int kKind>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_kv_k,
@@ -285,6 +299,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     __shared__ float red_l[2][kBM];        // [warpgroup][row]: half-row sums
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int kind = kKind == kKindAny ? P.kind : kKind;
     const int G = P.G, tq = kBM / G;
     const int units = P.Hkv * P.B;
     const int qtile = P.n_qtiles - 1 - static_cast<int>(blockIdx.x) / units;  // longest first
@@ -324,16 +339,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // Absolute indices: queries t0..t_end-1 of the chunk sit at start + t.
     int start = 0;
     bool skip = false;
-    if constexpr (kFromCache) {
+    if constexpr (kSrc != kKvFromQkv) {
         start = P.start[b];
-        skip = start < 0 || (P.kind == kLayerFull && static_cast<long long>(start) + P.T > P.cap);
+        skip = start < 0 || (kind == kLayerFull && static_cast<long long>(start) + P.T > P.cap);
         if (skip && tid == 0 && qtile == P.n_qtiles - 1 && g == 0) atomicOr(P.status, kErrPosition);
     }
     const int a0 = start + t0;
     // a ring is read in 128-key tiles aligned to its 128-slot boundaries, so
     // that no tile wraps around the end of the ring
-    const KeyTiles kt = prefill_key_tiles(P.kind, P.window, a0, start + t_end, kBN,
-                                          kFromCache && P.kind == kLayerSliding);
+    const KeyTiles kt = prefill_key_tiles(kind, P.window, a0, start + t_end, kBN,
+                                          kSrc == kKvFromRing);
     const int kv_lo = kt.kv_lo;
     const int ntiles = skip ? 0 : kt.ntiles;
 
@@ -373,9 +388,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     int slot;
                     if (!next_slot(slot)) return false;
                     uint8_t *dst = ring + slot * kSlotBytes;
-                    if constexpr (kFromCache) {
-                        const int slot0 = (P.kind == kLayerSliding)
-                                              ? static_cast<int>(key0 % P.cap) : key0;
+                    if constexpr (kSrc != kKvFromQkv) {
+                        const int slot0 =
+                            kSrc == kKvFromRing ? key0 % static_cast<int>(P.cap) : key0;
                         tma_load_4d(dst, &tm_kv_k, &bars[kBarSlotFull + slot], c * 64, slot0, g,
                                     b);
                     } else if (c * 64 < P.rot_w) {
@@ -395,9 +410,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     int slot;
                     if (!next_slot(slot)) return false;
                     uint8_t *dst = ring + slot * kSlotBytes;
-                    if constexpr (kFromCache) {
-                        const int slot0 = (P.kind == kLayerSliding)
-                                              ? static_cast<int>(key0 % P.cap) : key0;
+                    if constexpr (kSrc != kKvFromQkv) {
+                        const int slot0 =
+                            kSrc == kKvFromRing ? key0 % static_cast<int>(P.cap) : key0;
 #pragma unroll
                         for (int c = 0; c < 4; ++c)
                             tma_load_4d(dst + c * (kSlotBytes / 4), &tm_kv_v,
@@ -564,10 +579,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
             for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(sv[c]);
             const int key0 = kv_lo + j * kBN;
-            if (tile_needs_mask(P.kind, P.window, key0, kBN, a0, a_last)) {
+            if (tile_needs_mask(kind, P.window, key0, kBN, a0, a_last)) {
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
-                    const bool vis = key_visible(P.kind, P.window, tok_abs, key0 + col0 + c);
+                    const bool vis = key_visible(kind, P.window, tok_abs, key0 + col0 + c);
                     x[c] = vis ? x[c] : -INFINITY;
                 }
             }
@@ -697,12 +712,14 @@ cudaError_t launch_prefill(const CUtensorMap &tm_q, const CUtensorMap &tm_kv_k,
         err = launch_overlapped(cache_zero_tail_kernel, dim3(P.B), dim3(kRopeThreads), 0, stream,
                                 P);
         if (err != cudaSuccess) return err;
-        err = cudaFuncSetAttribute(prefill_attn_kernel<true>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmemBytes);
+        auto kernel = P.kind == kLayerSliding
+                          ? prefill_attn_kernel<kKvFromRing, kLayerSliding>
+                          : prefill_attn_kernel<kKvFromCache, kLayerFull>;
+        err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   kAttnSmemBytes);
         if (err != cudaSuccess) return err;
-        return launch_overlapped(prefill_attn_kernel<true>, dim3(grid), dim3(kAttnThreads),
-                                 kAttnSmemBytes, stream, tm_q, tm_kv_k, tm_kv_v, tm_krot, tm_out,
-                                 P);
+        return launch_overlapped(kernel, dim3(grid), dim3(kAttnThreads), kAttnSmemBytes, stream,
+                                 tm_q, tm_kv_k, tm_kv_v, tm_krot, tm_out, P);
     }
     if (P.rot_w > 0) {
         const long long items = r / 16 + (P.rot_w - r) / 8;
@@ -712,11 +729,13 @@ cudaError_t launch_prefill(const CUtensorMap &tm_q, const CUtensorMap &tm_kv_k,
                                 dim3(kRopeThreads), 0, stream, P);
         if (err != cudaSuccess) return err;
     }
-    err = cudaFuncSetAttribute(prefill_attn_kernel<false>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmemBytes);
+    auto kernel = P.kind == kLayerSliding ? prefill_attn_kernel<kKvFromQkv, kLayerSliding>
+                                          : prefill_attn_kernel<kKvFromQkv, kKindAny>;
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kAttnSmemBytes);
     if (err != cudaSuccess) return err;
-    err = launch_overlapped(prefill_attn_kernel<false>, dim3(grid), dim3(kAttnThreads),
-                            kAttnSmemBytes, stream, tm_q, tm_kv_k, tm_kv_v, tm_krot, tm_out, P);
+    err = launch_overlapped(kernel, dim3(grid), dim3(kAttnThreads), kAttnSmemBytes, stream, tm_q,
+                            tm_kv_k, tm_kv_v, tm_krot, tm_out, P);
     if (err != cudaSuccess || P.k_cache == nullptr) return err;
     // fill the decode cache (it reads only qkv and pos)
     return launch_overlapped(prefill_store_kv_kernel, dim3(static_cast<unsigned>(store_blocks)),
