@@ -311,13 +311,23 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant__ DecodeParams P) {
+// Warps per query head in the merge (each takes every kMergeWarps-th split),
+// and the largest group the shared reduction buffers hold.
+constexpr int kMergeWarps = 4;
+constexpr int kMergeMaxG = 8;
+int merge_warps(int G) { return G <= 4 ? kMergeWarps : 2; }
+
+__global__ void __launch_bounds__(512) decode_merge_kernel(const __grid_constant__ DecodeParams P) {
+    __shared__ float red_acc[kMergeMaxG][kMergeWarps - 1][kHeadDim];
+    __shared__ float red_l[kMergeMaxG][kMergeWarps - 1];
     const int g = blockIdx.x, b = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    grid_dep_wait();  // partial states of the split kernel
-    grid_dep_launch();
-    if (warp >= P.G) return;
-    const int h = g * P.G + warp;
+    const int S = static_cast<int>(blockDim.x) / (32 * P.G);  // warps per head
+    const int hq = warp / S, part = warp % S;  // head within the group, split phase
+    const int h = g * P.G + hq;
+    // The new token's q, k and v are inputs of the split kernel, which waited
+    // for them before letting this kernel start: rotate and score the token
+    // while the split kernel still runs.
     const long long p = P.pos[b];
     if (p < 0 || (P.kind == kLayerFull && p >= P.cap)) {
         if (g == 0 && threadIdx.x == 0) atomicOr(P.status, kErrPosition);
@@ -387,8 +397,12 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant
     for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
     const float x_new = dot * kScaleLog2;
 
+    grid_dep_wait();  // partial states of the split kernel
+    grid_dep_launch();
+
     // merge the new token with the partial states of the non-empty splits:
-    // the maximum lane-parallel, then the weighted sums, several splits in flight
+    // the maximum lane-parallel, then the weighted sums, the S warps of a head
+    // on interleaved splits with several in flight each
     const long long n_scan = decode_scan_slots(P.kind, p, P.cap);
     const int nvalid = static_cast<int>((n_scan + P.chunk - 1) / P.chunk);
     const size_t part0 = (static_cast<size_t>(b) * P.H + h) * P.nsplit;
@@ -396,13 +410,13 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant
     for (int sp = lane; sp < nvalid; sp += 32) M = fmaxf(M, P.part_ml[2 * (part0 + sp)]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    const float w_new = fast_exp2(x_new - M);
+    const float w_new = part == 0 ? fast_exp2(x_new - M) : 0.f;
     float L = w_new;
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = v[i] * w_new;
 #pragma unroll 4
-    for (int sp = 0; sp < nvalid; ++sp) {
+    for (int sp = part; sp < nvalid; sp += S) {
         const float2 ml = *reinterpret_cast<const float2 *>(P.part_ml + 2 * (part0 + sp));
         const float w = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
         L += ml.y * w;
@@ -417,6 +431,27 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant
         acc[6] += c.z * w;
         acc[7] += c.w * w;
     }
+    if (part > 0) {
+        float4 *dst = reinterpret_cast<float4 *>(&red_acc[hq][part - 1][d0]);
+        dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        if (lane == 0) red_l[hq][part - 1] = L;
+    }
+    __syncthreads();
+    if (part > 0) return;
+    for (int w = 0; w + 1 < S; ++w) {
+        const float4 *src = reinterpret_cast<const float4 *>(&red_acc[hq][w][d0]);
+        const float4 a = src[0], c = src[1];
+        acc[0] += a.x;
+        acc[1] += a.y;
+        acc[2] += a.z;
+        acc[3] += a.w;
+        acc[4] += c.x;
+        acc[5] += c.y;
+        acc[6] += c.z;
+        acc[7] += c.w;
+        L += red_l[hq][w];
+    }
     const float scale = gate_act(P.gate[static_cast<size_t>(b) * P.H + h], P.gate_mode) / L;
     uint4 ov;
     ov.x = pack_bf16x2(acc[0] * scale, acc[1] * scale);
@@ -427,7 +462,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const __grid_constant
                                static_cast<size_t>(h) * kHeadDim + d0) = ov;
 
     // write-then-attend: the new rotated key and its value go to slot(pos)
-    if (warp == 0) {
+    if (hq == 0) {
         const long long slot = (P.kind == kLayerFull) ? p : p % P.cap;
         const size_t off = ((static_cast<size_t>(b) * P.Hkv + g) * P.cap + slot) * kHeadDim + d0;
         *reinterpret_cast<uint4 *>(P.k_cache + off) = make_uint4(kb[0], kb[1], kb[2], kb[3]);
@@ -447,8 +482,8 @@ cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, cons
     err = launch_overlapped(decode_split_kernel, grid, dim3(kDecThreads), kDecSmemBytes, stream,
                             tm_k, tm_v, P);
     if (err != cudaSuccess) return err;
-    return launch_overlapped(decode_merge_kernel, dim3(P.Hkv, P.B), dim3(32 * P.G), 0, stream,
-                             P);
+    return launch_overlapped(decode_merge_kernel, dim3(P.Hkv, P.B),
+                             dim3(32 * P.G * merge_warps(P.G)), 0, stream, P);
 }
 
 }  // namespace spark
