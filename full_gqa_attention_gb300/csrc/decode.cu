@@ -24,20 +24,26 @@
 namespace spark {
 
 constexpr int kDecTile = 64;                              // cache slots per stage
-constexpr int kDecStages = 3;
+// TMA stages of a CTA: three for long scans; one where a CTA scans at most
+// kDecShortTiles tiles (rings), so that two CTAs fit on an SM and the grid of a
+// batch of rings runs as one wave.
+constexpr int kDecStagesLong = 3;
+constexpr int kDecShortTiles = 8;
 constexpr int kDecWarps = 4;                              // consumers, 16 slots each
 constexpr int kDecThreads = (kDecWarps + 1) * 32;         // + one producer warp
 constexpr int kDecTileBytes = kDecTile * kHeadDim * 2;    // 32 KB (K or V)
 constexpr int kDecStageBytes = 2 * kDecTileBytes;         // K + V
 constexpr int kDecQBytes = 8 * kHeadDim * 2;              // 8 (padded) query heads
-constexpr int kDecSmemBytes = 1024 + kDecStages * kDecStageBytes + kDecQBytes +
-                              2 * kDecStages * 8;
+constexpr int dec_smem_bytes(int stages) {
+    return 1024 + stages * kDecStageBytes + kDecQBytes + 2 * stages * 8;
+}
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-__global__ void __launch_bounds__(kDecThreads, 1)
+template <int kDecStages>
+__global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
                         const __grid_constant__ DecodeParams P) {
@@ -474,13 +480,14 @@ __global__ void __launch_bounds__(512) decode_merge_kernel(const __grid_constant
 
 cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeParams &P,
                           cudaStream_t stream) {
-    cudaError_t err = cudaFuncSetAttribute(decode_split_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           kDecSmemBytes);
+    const bool short_scan = P.chunk <= kDecShortTiles * kDecTile;
+    auto kernel = short_scan ? decode_split_kernel<1> : decode_split_kernel<kDecStagesLong>;
+    const int smem = dec_smem_bytes(short_scan ? 1 : kDecStagesLong);
+    cudaError_t err =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     dim3 grid(P.nsplit, P.Hkv, P.B);
-    err = launch_overlapped(decode_split_kernel, grid, dim3(kDecThreads), kDecSmemBytes, stream,
-                            tm_k, tm_v, P);
+    err = launch_overlapped(kernel, grid, dim3(kDecThreads), smem, stream, tm_k, tm_v, P);
     if (err != cudaSuccess) return err;
     return launch_overlapped(decode_merge_kernel, dim3(P.Hkv, P.B),
                              dim3(32 * P.G * merge_warps(P.G)), 0, stream, P);
