@@ -113,6 +113,9 @@ struct PrefillParams {
     int n_qtiles;              // query tiles per (b, kv head)
     int wave;                  // CTAs resident at once (one per SM): a CTA pulls the
                                // query tile of CTA blockIdx + wave into L2
+    int defer_wait;            // nonzero: a library kernel of the same call runs just
+                               // before the attention kernel, so only the key/value
+                               // loads wait for it (inputs are complete already)
     RopeTable rope;
 };
 

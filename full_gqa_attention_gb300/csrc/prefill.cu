@@ -334,7 +334,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
-    grid_dep_wait();  // rotated K (previous kernel) and every input are ready
+    // Programmatic dependent launch.  The kernel before this one may still run.
+    // When it is one of this call's own (rotated K, or the chunk's cache store),
+    // it waited for the call's inputs before letting this kernel start, so only
+    // the producer waits, before its first key/value load.  Otherwise every
+    // thread waits here, before reading any input.
+    if (!P.defer_wait) grid_dep_wait();
 
     // Absolute indices: queries t0..t_end-1 of the chunk sit at start + t.
     int start = 0;
@@ -372,6 +377,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int c = 0; c < 4; ++c)
                     tma_prefetch_l2_4d(&tm_q, c * 64, (nrem % P.Hkv) * G, nq * tq, nrem / P.Hkv);
             }
+            if (P.defer_wait) grid_dep_wait();  // rotated K / the cache are ready
             bool ok = true;
             auto next_slot = [&](int &slot) -> bool {
                 slot = sc % kSlots;
@@ -694,8 +700,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
 cudaError_t launch_prefill(const CUtensorMap &tm_q, const CUtensorMap &tm_kv_k,
                            const CUtensorMap &tm_kv_v, const CUtensorMap &tm_krot,
-                           const CUtensorMap &tm_out, const PrefillParams &P,
+                           const CUtensorMap &tm_out, const PrefillParams &P_in,
                            cudaStream_t stream) {
+    PrefillParams P = P_in;
+    // a library kernel runs before the attention kernel on every path but the
+    // one-shot prefill without rotated dims
+    P.defer_wait = (P.start != nullptr || P.rot_w > 0) ? 1 : 0;
     const int r = P.rope.rot_dim;
     const long long store_items = r / 16 + (kHeadDim - r) / 8 + kHeadDim / 8;
     const long long store_blocks =
