@@ -279,7 +279,10 @@ enum KvSource : int { kKvFromQkv = 0, kKvFromCache = 1, kKvFromRing = 2 };
 // the generic one for the one-shot full layer.
 constexpr int kKindAny = -1;
 
-template <int kSrc, int kKind>
+// kG: the GQA group size when fixed at compile time (the Spark-X2.5 shapes
+// all use 4), 0 to read it from P.G.  Timing chose the fixed size for the
+// sliding-kind kernels only; the full-kind ones measured faster without it.
+template <int kSrc, int kKind, int kG>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_kv_k,
@@ -300,7 +303,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int kind = kKind == kKindAny ? P.kind : kKind;
-    const int G = P.G, tq = kBM / G;
+    const int G = kG > 0 ? kG : P.G, tq = kBM / G;
     const int units = P.Hkv * P.B;
     const int qtile = P.n_qtiles - 1 - static_cast<int>(blockIdx.x) / units;  // longest first
     const int rem = static_cast<int>(blockIdx.x) % units;
@@ -554,11 +557,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // two warpgroups take alternate groups of 8 pairs, and the G rows of a
         // token (adjacent lanes) share the angles
         if (ok) {
-            switch (G) {
-                case 1: rotate_q_row<1>(qbuf, row, lane, wg, p, P.rope); break;
-                case 2: rotate_q_row<2>(qbuf, row, lane, wg, p, P.rope); break;
-                case 4: rotate_q_row<4>(qbuf, row, lane, wg, p, P.rope); break;
-                default: rotate_q_row<8>(qbuf, row, lane, wg, p, P.rope); break;
+            if constexpr (kG > 0) {
+                rotate_q_row<kG>(qbuf, row, lane, wg, p, P.rope);
+            } else {
+                switch (G) {
+                    case 1: rotate_q_row<1>(qbuf, row, lane, wg, p, P.rope); break;
+                    case 2: rotate_q_row<2>(qbuf, row, lane, wg, p, P.rope); break;
+                    case 4: rotate_q_row<4>(qbuf, row, lane, wg, p, P.rope); break;
+                    default: rotate_q_row<8>(qbuf, row, lane, wg, p, P.rope); break;
+                }
             }
         }
         fence_proxy_async_smem();
@@ -698,6 +705,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
 // ---------------------------------------------------------------- launcher
 
+// The attention kernel for a KV source and layer kind; sliding-kind kernels
+// are specialised for a group of 4.
+template <int kSrc, int kKind>
+auto attn_kernel_for(int G) {
+    if constexpr (kKind == kLayerSliding)
+        return G == 4 ? prefill_attn_kernel<kSrc, kKind, 4> : prefill_attn_kernel<kSrc, kKind, 0>;
+    else
+        return prefill_attn_kernel<kSrc, kKind, 0>;
+}
+
 cudaError_t launch_prefill(const CUtensorMap &tm_q, const CUtensorMap &tm_kv_k,
                            const CUtensorMap &tm_kv_v, const CUtensorMap &tm_krot,
                            const CUtensorMap &tm_out, const PrefillParams &P_in,
@@ -723,8 +740,8 @@ cudaError_t launch_prefill(const CUtensorMap &tm_q, const CUtensorMap &tm_kv_k,
                                 P);
         if (err != cudaSuccess) return err;
         auto kernel = P.kind == kLayerSliding
-                          ? prefill_attn_kernel<kKvFromRing, kLayerSliding>
-                          : prefill_attn_kernel<kKvFromCache, kLayerFull>;
+                          ? attn_kernel_for<kKvFromRing, kLayerSliding>(P.G)
+                          : attn_kernel_for<kKvFromCache, kLayerFull>(P.G);
         err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    kAttnSmemBytes);
         if (err != cudaSuccess) return err;
@@ -739,8 +756,8 @@ cudaError_t launch_prefill(const CUtensorMap &tm_q, const CUtensorMap &tm_kv_k,
                                 dim3(kRopeThreads), 0, stream, P);
         if (err != cudaSuccess) return err;
     }
-    auto kernel = P.kind == kLayerSliding ? prefill_attn_kernel<kKvFromQkv, kLayerSliding>
-                                          : prefill_attn_kernel<kKvFromQkv, kKindAny>;
+    auto kernel = P.kind == kLayerSliding ? attn_kernel_for<kKvFromQkv, kLayerSliding>(P.G)
+                                          : attn_kernel_for<kKvFromQkv, kKindAny>(P.G);
     err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kAttnSmemBytes);
     if (err != cudaSuccess) return err;
