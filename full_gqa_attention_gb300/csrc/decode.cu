@@ -74,17 +74,33 @@ __global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
     if (c_lo >= c_hi) return;  // empty split: the merge does not read it
     const int ntiles = static_cast<int>((c_hi - c_lo + kDecTile - 1) / kDecTile);
 
-    if (tid == 0) {
+    // one tile of K and V into stage t % kDecStages
+    auto issue_tile = [&](int t) {
+        const int s = t % kDecStages;
+        mbar_arrive_expect_tx(&full[s], kDecStageBytes);
+        const int key0 = static_cast<int>(c_lo + static_cast<long long>(t) * kDecTile);
+        uint8_t *kt = stages + s * kDecStageBytes;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            tma_load_4d(kt + c * (kDecTileBytes / 4), &tm_k, &full[s], c * 64, key0, g, b);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            tma_load_4d(kt + kDecTileBytes + c * (kDecTileBytes / 4), &tm_v, &full[s], c * 64,
+                        key0, g, b);
+    };
+    // The producer sets the stages up and starts the first loads at once: they
+    // do not depend on the query prologue below, which they overlap.
+    const int n_pre = ntiles < kDecStages ? ntiles : kDecStages;
+    if (tid == kDecWarps * 32) {
         for (int s = 0; s < kDecStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kDecWarps);
         }
         fence_mbar_init();
         abort_flag = 0;
-    }
-    if (warp == kDecWarps && lane == 0) {
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
+        for (int t = 0; t < n_pre; ++t) issue_tile(t);
     }
 
     // The group's G query heads, rotated and rounded to bf16 (heads G..7 zero).
@@ -115,23 +131,13 @@ __global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
 
     if (warp == kDecWarps) {
         // ------------------------------------------------------ TMA producer
-        int issued = 0;
+        int issued = n_pre;
         if (lane == 0) {
-            for (int t = 0; t < ntiles; ++t) {
-                const int s = t % kDecStages;
-                if (t >= kDecStages &&
-                    !mbar_wait(&empty[s], ((t / kDecStages) - 1) & 1, &abort_flag, P.status))
+            for (int t = n_pre; t < ntiles; ++t) {
+                if (!mbar_wait(&empty[t % kDecStages], ((t / kDecStages) - 1) & 1, &abort_flag,
+                               P.status))
                     break;
-                mbar_arrive_expect_tx(&full[s], kDecStageBytes);
-                const int key0 = static_cast<int>(c_lo + static_cast<long long>(t) * kDecTile);
-                uint8_t *kt = stages + s * kDecStageBytes;
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    tma_load_4d(kt + c * (kDecTileBytes / 4), &tm_k, &full[s], c * 64, key0, g, b);
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    tma_load_4d(kt + kDecTileBytes + c * (kDecTileBytes / 4), &tm_v, &full[s],
-                                c * 64, key0, g, b);
+                issue_tile(t);
                 ++issued;
             }
         }
