@@ -74,6 +74,13 @@ def test_sliding_ring_512(cuda, positions):
     run_case(cuda, wl.SLIDING_LAYER, 16, 4, 512, positions, seed=2)
 
 
+def test_ring_positions_at_the_limit(cuda):
+    """Ring decode at positions up to 2^24 - 1 (the largest accepted): the
+    new token's angles turn ~1.7e7 rad and its slot is pos mod 512."""
+    top = (1 << 24) - 1
+    run_case(cuda, wl.SLIDING_LAYER, 16, 4, 512, [top, top - 1, top - 511, top - 512], seed=31)
+
+
 def test_ring_larger_than_window(cuda):
     run_case(cuda, wl.SLIDING_LAYER, 16, 4, 600, [100, 599, 600, 601, 1799, 2000], seed=3)
 

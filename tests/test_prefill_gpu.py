@@ -119,6 +119,20 @@ def test_large_positions(cuda):
     run(cuda, case, positions=torch.tensor(rng.integers(0, 1 << 20, (1, 200)), dtype=torch.int32))
 
 
+@pytest.mark.parametrize("layer", [wl.FULL_LAYER, wl.SLIDING_LAYER])
+def test_positions_at_the_limit(cuda, layer):
+    """Positions up to 2^24 - 1, the largest the library accepts: the highest
+    frequency turns ~1.7e7 rad, where an fp32 angle would have lost every
+    digit; descending and repeated positions are valid too."""
+    case = wl.PrefillCase("poslim", B=2, T=160, H=8, Hkv=2, layer=layer, seed=7)
+    top = (1 << 24) - 1
+    positions = torch.stack([
+        top - 159 + torch.arange(160, dtype=torch.int32),        # the last 160 positions
+        torch.full((160,), top, dtype=torch.int32) - torch.arange(160, dtype=torch.int32) % 7,
+    ])
+    run(cuda, case, positions=positions)
+
+
 @pytest.mark.parametrize("T,W,H,Hkv", [(513, 512, 8, 2), (257, 256, 8, 2), (1025, 512, 16, 4),
                                        (513, 512, 8, 8), (513, 512, 16, 2)])
 def test_unmasked_last_tile_repeatable(cuda, T, W, H, Hkv):
