@@ -85,8 +85,19 @@ def test_chunked_prefill(cuda, kind, T, cap, poison):
     more tokens in one call (ragged start); the chunk's rows equal the oracle's
     rows of a prefill over the whole sequence, and a decode of the next token
     continues it.  With `poison`, slots never written hold NaN."""
+    _chunked(cuda, kind, T, cap, poison, 16, 4)
+
+
+@pytest.mark.parametrize("kind,cap", [(FULL, 2048), (SLIDING, 768)])
+@pytest.mark.parametrize("H,Hkv", [(8, 8), (16, 2)])
+def test_chunked_prefill_group_sizes(cuda, kind, cap, H, Hkv):
+    """The chunked prefill with groups of 1 and 8 query heads per KV head (the
+    kernels built for other group sizes than the models' 4)."""
+    _chunked(cuda, kind, 200, cap, False, H, Hkv)
+
+
+def _chunked(cuda, kind, T, cap, poison, H, Hkv):
     layer = wl.FULL_LAYER if kind == FULL else wl.SLIDING_LAYER
-    H, Hkv = 16, 4
     starts = [300, 700]
     total = max(starts) + T + 1
     case = wl.PrefillCase("chunk", B=2, T=total, H=H, Hkv=Hkv, layer=layer, seed=T + cap)
