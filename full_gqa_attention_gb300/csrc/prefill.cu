@@ -458,8 +458,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // ------------------------------------------------------ MMA issuer
         if (lane == 0 && !skip) {
             int sc = 0;
-            const uint32_t q_addr = smem_u32(qbuf);
-            const uint32_t ring_addr = smem_u32(ring);
+            // Shared-memory descriptors built once: the address field holds
+            // (address mod 2^18) / 16 in its low bits, and every operand lies
+            // below 2^18, so an operand at byte offset o from a base has the
+            // base's descriptor plus o / 16.  This keeps the issue loop short.
+            const uint64_t q_desc = smem_desc_sw128(smem_u32(qbuf), 16, 1024);
+            const uint64_t k_desc = smem_desc_sw128(smem_u32(ring), 16, 1024);
+            const uint64_t v_desc = smem_desc_sw128(smem_u32(ring), kSlotBytes / 4, 1024);
+            // (the full-layer cache instance measured faster building each
+            // descriptor in place)
+            constexpr bool kDescInPlace = kSrc == kKvFromCache;
+            const uint32_t q_addr = smem_u32(qbuf), ring_addr = smem_u32(ring);
             bool ok = mbar_wait(&bars[kBarQReady], 0, &abort_flag, P.status);
             tc_fence_after();
             auto mma_qk = [&](int j) -> bool {
@@ -472,8 +481,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = smem_desc_sw128(q_addr + c * kSlotBytes + kk * 32, 16, 1024);
-                        const uint64_t bd = smem_desc_sw128(ring_addr + slot * kSlotBytes + kk * 32, 16, 1024);
+                        const uint64_t ad =
+                            kDescInPlace
+                                ? smem_desc_sw128(q_addr + c * kSlotBytes + kk * 32, 16, 1024)
+                                : q_desc + static_cast<uint32_t>((c * kSlotBytes + kk * 32) >> 4);
+                        const uint64_t bd =
+                            kDescInPlace
+                                ? smem_desc_sw128(ring_addr + slot * kSlotBytes + kk * 32, 16, 1024)
+                                : k_desc + static_cast<uint32_t>((slot * kSlotBytes + kk * 32) >> 4);
                         mma_ss(d, ad, bd, kIdescQK, (c | kk) != 0);
                     }
                     tc_commit(&bars[kBarSlotEmpty + slot]);
@@ -493,8 +508,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk) {
                         const int ks = vs * 2 + kk;  // 16-key step within the tile
-                        const uint64_t bd = smem_desc_sw128(ring_addr + slot * kSlotBytes + kk * 2048,
-                                                            kSlotBytes / 4, 1024);
+                        const uint64_t bd =
+                            kDescInPlace
+                                ? smem_desc_sw128(ring_addr + slot * kSlotBytes + kk * 2048,
+                                                  kSlotBytes / 4, 1024)
+                                : v_desc + static_cast<uint32_t>((slot * kSlotBytes + kk * 2048) >> 4);
                         // P of keys 0..63 sits in packed columns 0..31, keys 64..127 in 64..95
                         const uint32_t acol = pcol + (ks < 4 ? ks * 8 : 64 + (ks - 4) * 8);
                         mma_ts(tmem + kColO, acol, bd, kIdescPV, (j > 0 || ks > 0));
