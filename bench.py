@@ -744,10 +744,10 @@ def time_other_configs(fga, dev, bf16_peak, hbm_peak):
 # current kernels, scaled to one launch of the bench workload; None when the
 # kernels changed since the counters were taken.
 # decode_split_kernel: 540.5 MB in a 131,072-token capture, scaled x8 to the
-# 1,048,576-token layer; prefill_attn_kernel: 491.8 MB measured on this workload.
+# 1,048,576-token layer; prefill_attn_kernel: 492.2 MB measured on this workload.
 TRAFFIC: dict[str, float | None] = {
     "decode_split_kernel": 540.474624e6 * 8,
-    "prefill_attn_kernel": 491.791872e6,
+    "prefill_attn_kernel": 492.185344e6,
 }
 
 
