@@ -90,8 +90,26 @@ struct DecodeParams {
     int gate_mode;             // 0 sigmoid, 1 silu
     int nsplit;                // splits per (b, kv head)
     int chunk;                 // scanned slots per split (multiple of 64)
+    // 1: the split kernel merges (no merge kernel).  With several splits per
+    // (b, kv head) the CTA that finishes last does it, found by counting the
+    // finished splits in counters[b * Hkv + g], which every call leaves at 0.
+    int fuse_merge;
+    unsigned *counters;        // [B * Hkv] when fuse_merge and nsplit > 1
     RopeTable rope;
 };
+
+// Whether a decode call merges inside the split kernel.  One warp per head of
+// the finishing CTA walks every split, so this pays only for a few splits
+// (rings, short caches): at most kFuseMaxSplits.  With more than one split
+// the finished splits are counted in the workspace header, in the words after
+// the status word, one per (sequence, KV head); every call leaves them at 0.
+constexpr int kFuseMaxSplits = 8;
+constexpr int kHeaderCounters = static_cast<int>(kWorkspaceHeader / sizeof(unsigned)) - 1;
+
+inline bool decode_fuses_merge(int nsplit, long long B_times_Hkv, bool have_counters) {
+    if (nsplit == 1) return true;
+    return have_counters && nsplit <= kFuseMaxSplits && B_times_Hkv <= kHeaderCounters;
+}
 
 // ---------------------------------------------------------------- prefill
 

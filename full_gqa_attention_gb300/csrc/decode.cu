@@ -15,6 +15,10 @@
 //   decode_merge_kernel  grid (Hkv, B).  Rotates q and the new key, scores the
 //       new token, merges it with the partial states (log-sum-exp rescale),
 //       applies the gate, and stores the new key/value at slot(pos).
+// When a (sequence, KV head) has at most kFuseMaxSplits splits (rings, short
+// caches) the split kernel does the merge itself, with the same arithmetic:
+// the CTA that finishes last (a counter of finished splits in the workspace)
+// merges the states, so the step is one launch instead of two.
 // The new token is not read from the cache by the split kernel, so the cache
 // write can come last without a race: on a full layer slot(pos) lies past
 // every cached token, and on a ring it holds token pos - cap, which is out of
@@ -42,7 +46,196 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-template <int kDecStages>
+// Warps per query head in the merge (each takes every S-th split), and the
+// largest group the merge kernel's shared reduction buffers hold.
+constexpr int kMergeWarps = 4;
+constexpr int kMergeMaxG = 8;
+__host__ __device__ constexpr int merge_warps(int G) { return G <= 4 ? kMergeWarps : 2; }
+
+// The new token seen by query head h of KV head g: q and the new key rotated
+// at pos and rounded to bf16, the score x_new = q.k_new / 16 in base-2 units,
+// and this lane's 8 dims of v_new.  Lane l holds dims 8l..8l+7; the rotated
+// key is kept packed (bf16) for the cache store.
+struct NewToken {
+    float x_new;
+    float v[8];
+    uint32_t kb[4];
+    uint4 vv;
+};
+
+__device__ __forceinline__ NewToken score_new_token(const DecodeParams &P, int b, int g, int h,
+                                                    long long p, int lane) {
+    NewToken nt;
+    const size_t width = static_cast<size_t>(P.H + 2 * P.Hkv) * kHeadDim;
+    const __nv_bfloat16 *row = P.qkv + b * width;
+    const uint4 qv = *reinterpret_cast<const uint4 *>(row + static_cast<size_t>(h) * kHeadDim + lane * 8);
+    const uint4 kv = *reinterpret_cast<const uint4 *>(row + static_cast<size_t>(P.H + g) * kHeadDim + lane * 8);
+    nt.vv = *reinterpret_cast<const uint4 *>(row + static_cast<size_t>(P.H + P.Hkv + g) * kHeadDim + lane * 8);
+    const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+    const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
+    const uint32_t vw[4] = {nt.vv.x, nt.vv.y, nt.vv.z, nt.vv.w};
+    float q[8], k[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        q[2 * i] = bf16_lo(qw[i]);
+        q[2 * i + 1] = bf16_hi(qw[i]);
+        k[2 * i] = bf16_lo(kw[i]);
+        k[2 * i + 1] = bf16_hi(kw[i]);
+        nt.v[2 * i] = bf16_lo(vw[i]);
+        nt.v[2 * i + 1] = bf16_hi(vw[i]);
+    }
+
+    // RoPE of this lane's 8 dims d0..d0+7; the partner dims d -/+ r/2 live in
+    // the lane r/16 away (r/2 is a multiple of 8).
+    const int r = P.rope.rot_dim, half = r / 2, d0 = lane * 8;
+    if (r > 0) {
+        const int partner = (d0 >= r) ? lane : (d0 < half ? lane + half / 8 : lane - half / 8);
+        float qp[8], kp[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            qp[i] = __shfl_sync(0xffffffffu, q[i], partner);
+            kp[i] = __shfl_sync(0xffffffffu, k[i], partner);
+        }
+        if (d0 < r) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int kk = (d0 < half) ? d0 + i : d0 + i - half;
+                float c, s;
+                rope_cos_sin(static_cast<int>(p), P.rope.u[kk], c, s);
+                float y1, y2;
+                if (d0 < half) {
+                    rope_rotate(q[i], qp[i], c, s, y1, y2);
+                    q[i] = y1;
+                    rope_rotate(k[i], kp[i], c, s, y1, y2);
+                    k[i] = y1;
+                } else {
+                    rope_rotate(qp[i], q[i], c, s, y1, y2);
+                    q[i] = y2;
+                    rope_rotate(kp[i], k[i], c, s, y1, y2);
+                    k[i] = y2;
+                }
+            }
+        }
+    }
+    float dot = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        nt.kb[i] = pack_bf16x2(k[2 * i], k[2 * i + 1]);
+        const uint32_t qb = pack_bf16x2(q[2 * i], q[2 * i + 1]);
+        dot = fmaf(bf16_lo(qb), bf16_lo(nt.kb[i]), dot);
+        dot = fmaf(bf16_hi(qb), bf16_hi(nt.kb[i]), dot);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+    nt.x_new = dot * kScaleLog2;
+    return nt;
+}
+
+// Gated output of head h and, for the first head of the group, the new
+// key/value stored at slot(pos) (write-then-attend: no split reads that slot).
+__device__ __forceinline__ void store_head(const DecodeParams &P, int b, int g, int hq, int h,
+                                           long long p, int d0, const float (&acc)[8], float L,
+                                           const NewToken &nt) {
+    const float scale = gate_act(P.gate[static_cast<size_t>(b) * P.H + h], P.gate_mode) / L;
+    uint4 ov;
+    ov.x = pack_bf16x2(acc[0] * scale, acc[1] * scale);
+    ov.y = pack_bf16x2(acc[2] * scale, acc[3] * scale);
+    ov.z = pack_bf16x2(acc[4] * scale, acc[5] * scale);
+    ov.w = pack_bf16x2(acc[6] * scale, acc[7] * scale);
+    *reinterpret_cast<uint4 *>(P.out + static_cast<size_t>(b) * P.H * kHeadDim +
+                               static_cast<size_t>(h) * kHeadDim + d0) = ov;
+    if (hq == 0) {
+        const long long slot = (P.kind == kLayerFull) ? p : p % P.cap;
+        const size_t off = ((static_cast<size_t>(b) * P.Hkv + g) * P.cap + slot) * kHeadDim + d0;
+        *reinterpret_cast<uint4 *>(P.k_cache + off) = make_uint4(nt.kb[0], nt.kb[1], nt.kb[2], nt.kb[3]);
+        *reinterpret_cast<uint4 *>(P.v_cache + off) = nt.vv;
+    }
+}
+
+// Part sums of the merge for S parts (S = merge_warps(G), a template argument
+// so that the prefetched states stay in registers): part q sums the splits
+// q, q+S, ..., part 0 starting from the new token, then parts 1..S-1 are
+// added to part 0 in turn -- the merge kernel's order, where part q is its
+// warp q of the head.
+template <int S>
+__device__ __forceinline__ void merge_parts(const NewToken &nt, float M, int nvalid,
+                                            const float2 (&ml)[kFuseMaxSplits],
+                                            const float4 (&pa)[kFuseMaxSplits],
+                                            const float4 (&pc)[kFuseMaxSplits], float (&acc)[8],
+                                            float &L) {
+    const float w_new = fast_exp2(nt.x_new - M);
+#pragma unroll
+    for (int q = 0; q < S; ++q) {
+        const float wq = q == 0 ? w_new : 0.f;
+        float Lq = wq, aq[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) aq[i] = nt.v[i] * wq;
+#pragma unroll
+        for (int sp = q; sp < kFuseMaxSplits; sp += S) {
+            if (sp < nvalid) {
+                const float w = (ml[sp].x == -INFINITY) ? 0.f : fast_exp2(ml[sp].x - M);
+                Lq += ml[sp].y * w;
+                aq[0] += pa[sp].x * w;
+                aq[1] += pa[sp].y * w;
+                aq[2] += pa[sp].z * w;
+                aq[3] += pa[sp].w * w;
+                aq[4] += pc[sp].x * w;
+                aq[5] += pc[sp].y * w;
+                aq[6] += pc[sp].z * w;
+                aq[7] += pc[sp].w * w;
+            }
+        }
+        if (q == 0) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = aq[i];
+            L = Lq;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] += aq[i];
+            L += Lq;
+        }
+    }
+}
+
+// The merge of query head hq of the group, done by one warp of the split
+// kernel, with the same arithmetic in the same order as the merge kernel.
+// `nt` (the new token) was loaded before the split count; the states of all
+// (at most kFuseMaxSplits) splits are then fetched at once.  Other CTAs wrote
+// them, so they are read at L2 (ld.global.cg).
+__device__ __forceinline__ void merge_head_in_split(const DecodeParams &P, int b, int g, int hq,
+                                                    long long p, int nvalid, int lane,
+                                                    const NewToken &nt) {
+    const int h = g * P.G + hq, d0 = lane * 8;
+    const size_t part0 = (static_cast<size_t>(b) * P.H + h) * P.nsplit;
+    float2 ml[kFuseMaxSplits];
+    float4 pa[kFuseMaxSplits], pc[kFuseMaxSplits];
+#pragma unroll
+    for (int sp = 0; sp < kFuseMaxSplits; ++sp) {
+        if (sp < nvalid) {
+            ml[sp] = __ldcg(reinterpret_cast<const float2 *>(P.part_ml + 2 * (part0 + sp)));
+            const float4 *po = reinterpret_cast<const float4 *>(P.part_o + (part0 + sp) * kHeadDim + d0);
+            pa[sp] = __ldcg(po);
+            pc[sp] = __ldcg(po + 1);
+        } else {
+            ml[sp] = make_float2(-INFINITY, 0.f);
+            pa[sp] = pc[sp] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    // the maximum over the new token and every split (absent ones are -inf)
+    float M = nt.x_new;
+#pragma unroll
+    for (int sp = 0; sp < kFuseMaxSplits; ++sp) M = fmaxf(M, ml[sp].x);
+    float acc[8], L;
+    if (merge_warps(P.G) == kMergeWarps)
+        merge_parts<kMergeWarps>(nt, M, nvalid, ml, pa, pc, acc, L);
+    else
+        merge_parts<2>(nt, M, nvalid, ml, pa, pc, acc, L);
+    store_head(P, b, g, hq, h, p, d0, acc, L, nt);
+}
+
+// kFuse: this CTA's grid merges itself (P.fuse_merge); a separate
+// instantiation, so that the kernel of the long scans carries none of it.
+template <int kDecStages, bool kFuse>
 __global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
@@ -71,7 +264,16 @@ __global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
     const long long n_scan = decode_scan_slots(P.kind, p, P.cap);
     const long long c_lo = static_cast<long long>(split) * P.chunk;
     const long long c_hi = (c_lo + P.chunk < n_scan) ? c_lo + P.chunk : n_scan;
-    if (c_lo >= c_hi) return;  // empty split: the merge does not read it
+    if (c_lo >= c_hi) {
+        // An empty split: the merge does not read it.  With nothing cached yet
+        // no split has work, and a fused merge then comes from split 0, on the
+        // new token alone.
+        if (kFuse && n_scan == 0 && split == 0 && warp < kDecWarps)
+            for (int hq = warp; hq < P.G; hq += kDecWarps)
+                merge_head_in_split(P, b, g, hq, p, 0, lane,
+                                    score_new_token(P, b, g, g * P.G + hq, p, lane));
+        return;
+    }
     const int ntiles = static_cast<int>((c_hi - c_lo + kDecTile - 1) / kDecTile);
 
     // one tile of K and V into stage t % kDecStages
@@ -320,14 +522,44 @@ __global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
                                                          split)) = ml;
         }
     }
-    __syncthreads();
-}
+    if constexpr (!kFuse) {
+        __syncthreads();
+        return;
+    }
+    __syncthreads();  // the producer warp has returned after this barrier
 
-// Warps per query head in the merge (each takes every kMergeWarps-th split),
-// and the largest group the shared reduction buffers hold.
-constexpr int kMergeWarps = 4;
-constexpr int kMergeMaxG = 8;
-int merge_warps(int G) { return G <= 4 ? kMergeWarps : 2; }
+    // ---------------------------------------------------------- fused merge
+    // Every non-empty split counts itself once it has written its states (an
+    // aborted one too, so the count always completes and returns to 0); the
+    // one that completes the count merges.  No thread waits on another CTA.
+    const int nvalid = static_cast<int>((n_scan + P.chunk - 1) / P.chunk);
+    // The new token of this warp's heads (warp, warp + 4) first: its loads
+    // then overlap the count instead of following it.
+    NewToken nt[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int hq = warp + i * kDecWarps;
+        if (hq < P.G) nt[i] = score_new_token(P, b, g, g * P.G + hq, p, lane);
+    }
+    if (nvalid > 1) {
+        __shared__ int last_cta;
+        __threadfence();  // this thread's states are visible on the device before the count
+        named_bar_sync(1, kDecWarps * 32);
+        if (tid == 0) {
+            unsigned *cnt = P.counters + static_cast<size_t>(b) * P.Hkv + g;
+            last_cta = atomicAdd(cnt, 1u) == static_cast<unsigned>(nvalid - 1);
+            if (last_cta) atomicExch(cnt, 0u);  // every split has counted: reset for the next call
+        }
+        named_bar_sync(1, kDecWarps * 32);
+        if (!last_cta) return;
+        __threadfence();  // order the reads of the other splits' states after the count
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int hq = warp + i * kDecWarps;
+        if (hq < P.G) merge_head_in_split(P, b, g, hq, p, nvalid, lane, nt[i]);
+    }
+}
 
 __global__ void __launch_bounds__(512) decode_merge_kernel(const __grid_constant__ DecodeParams P) {
     __shared__ float red_acc[kMergeMaxG][kMergeWarps - 1][kHeadDim];
@@ -345,69 +577,10 @@ __global__ void __launch_bounds__(512) decode_merge_kernel(const __grid_constant
         if (g == 0 && threadIdx.x == 0) atomicOr(P.status, kErrPosition);
         return;
     }
-    const size_t width = static_cast<size_t>(P.H + 2 * P.Hkv) * kHeadDim;
-    const __nv_bfloat16 *row = P.qkv + b * width;
-    const uint4 qv = *reinterpret_cast<const uint4 *>(row + static_cast<size_t>(h) * kHeadDim + lane * 8);
-    const uint4 kv = *reinterpret_cast<const uint4 *>(row + static_cast<size_t>(P.H + g) * kHeadDim + lane * 8);
-    const uint4 vv = *reinterpret_cast<const uint4 *>(row + static_cast<size_t>(P.H + P.Hkv + g) * kHeadDim + lane * 8);
-    const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
-    const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
-    const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
-    float q[8], k[8], v[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        q[2 * i] = bf16_lo(qw[i]);
-        q[2 * i + 1] = bf16_hi(qw[i]);
-        k[2 * i] = bf16_lo(kw[i]);
-        k[2 * i + 1] = bf16_hi(kw[i]);
-        v[2 * i] = bf16_lo(vw[i]);
-        v[2 * i + 1] = bf16_hi(vw[i]);
-    }
-
-    // RoPE of this lane's 8 dims d0..d0+7; the partner dims d -/+ r/2 live in
-    // the lane r/16 away (r/2 is a multiple of 8).
-    const int r = P.rope.rot_dim, half = r / 2, d0 = lane * 8;
-    if (r > 0) {
-        const int partner = (d0 >= r) ? lane : (d0 < half ? lane + half / 8 : lane - half / 8);
-        float qp[8], kp[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            qp[i] = __shfl_sync(0xffffffffu, q[i], partner);
-            kp[i] = __shfl_sync(0xffffffffu, k[i], partner);
-        }
-        if (d0 < r) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int kk = (d0 < half) ? d0 + i : d0 + i - half;
-                float c, s;
-                rope_cos_sin(static_cast<int>(p), P.rope.u[kk], c, s);
-                float y1, y2;
-                if (d0 < half) {
-                    rope_rotate(q[i], qp[i], c, s, y1, y2);
-                    q[i] = y1;
-                    rope_rotate(k[i], kp[i], c, s, y1, y2);
-                    k[i] = y1;
-                } else {
-                    rope_rotate(qp[i], q[i], c, s, y1, y2);
-                    q[i] = y2;
-                    rope_rotate(kp[i], k[i], c, s, y1, y2);
-                    k[i] = y2;
-                }
-            }
-        }
-    }
-    uint32_t kb[4];
-    float dot = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        kb[i] = pack_bf16x2(k[2 * i], k[2 * i + 1]);
-        const uint32_t qb = pack_bf16x2(q[2 * i], q[2 * i + 1]);
-        dot = fmaf(bf16_lo(qb), bf16_lo(kb[i]), dot);
-        dot = fmaf(bf16_hi(qb), bf16_hi(kb[i]), dot);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-    const float x_new = dot * kScaleLog2;
+    const NewToken nt = score_new_token(P, b, g, h, p, lane);
+    const float x_new = nt.x_new;
+    const float *v = nt.v;
+    const int d0 = lane * 8;
 
     grid_dep_wait();  // partial states of the split kernel
     grid_dep_launch();
@@ -464,22 +637,7 @@ __global__ void __launch_bounds__(512) decode_merge_kernel(const __grid_constant
         acc[7] += c.w;
         L += red_l[hq][w];
     }
-    const float scale = gate_act(P.gate[static_cast<size_t>(b) * P.H + h], P.gate_mode) / L;
-    uint4 ov;
-    ov.x = pack_bf16x2(acc[0] * scale, acc[1] * scale);
-    ov.y = pack_bf16x2(acc[2] * scale, acc[3] * scale);
-    ov.z = pack_bf16x2(acc[4] * scale, acc[5] * scale);
-    ov.w = pack_bf16x2(acc[6] * scale, acc[7] * scale);
-    *reinterpret_cast<uint4 *>(P.out + static_cast<size_t>(b) * P.H * kHeadDim +
-                               static_cast<size_t>(h) * kHeadDim + d0) = ov;
-
-    // write-then-attend: the new rotated key and its value go to slot(pos)
-    if (hq == 0) {
-        const long long slot = (P.kind == kLayerFull) ? p : p % P.cap;
-        const size_t off = ((static_cast<size_t>(b) * P.Hkv + g) * P.cap + slot) * kHeadDim + d0;
-        *reinterpret_cast<uint4 *>(P.k_cache + off) = make_uint4(kb[0], kb[1], kb[2], kb[3]);
-        *reinterpret_cast<uint4 *>(P.v_cache + off) = vv;
-    }
+    store_head(P, b, g, hq, h, p, d0, acc, L, nt);
 }
 
 // ---------------------------------------------------------------- launchers
@@ -487,14 +645,17 @@ __global__ void __launch_bounds__(512) decode_merge_kernel(const __grid_constant
 cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeParams &P,
                           cudaStream_t stream) {
     const bool short_scan = P.chunk <= kDecShortTiles * kDecTile;
-    auto kernel = short_scan ? decode_split_kernel<1> : decode_split_kernel<kDecStagesLong>;
+    auto kernel = short_scan ? (P.fuse_merge ? decode_split_kernel<1, true>
+                                             : decode_split_kernel<1, false>)
+                             : (P.fuse_merge ? decode_split_kernel<kDecStagesLong, true>
+                                             : decode_split_kernel<kDecStagesLong, false>);
     const int smem = dec_smem_bytes(short_scan ? 1 : kDecStagesLong);
     cudaError_t err =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
     dim3 grid(P.nsplit, P.Hkv, P.B);
     err = launch_overlapped(kernel, grid, dim3(kDecThreads), smem, stream, tm_k, tm_v, P);
-    if (err != cudaSuccess) return err;
+    if (err != cudaSuccess || P.fuse_merge) return err;
     return launch_overlapped(decode_merge_kernel, dim3(P.Hkv, P.B),
                              dim3(32 * P.G * merge_warps(P.G)), 0, stream, P);
 }

@@ -386,6 +386,8 @@ spark_status decode_impl(const void *qkv, const float *gate, const int32_t *pos,
     P.gate_mode = desc->gate_mode;
     P.nsplit = pl.nsplit;
     P.chunk = pl.chunk;
+    P.counters = reinterpret_cast<unsigned *>(ws) + 1;  // header words after the status word
+    P.fuse_merge = decode_fuses_merge(pl.nsplit, static_cast<long long>(B) * Hkv, true) ? 1 : 0;
     make_rope_table(desc, &P.rope);
 
     // caches as [B][Hkv][cap][256]; boxes of 64 slots x 64 dims (128-byte rows)
@@ -594,6 +596,10 @@ extern "C" spark_status spark_attn_decode_noalloc(const void *qkv, const float *
     P.gate_mode = desc->gate_mode;
     P.nsplit = pl.nsplit;
     P.chunk = pl.chunk;
+    // the scratch buffer is never zeroed, so it holds no split counters: the
+    // split kernel merges only where it is the only split
+    P.counters = nullptr;
+    P.fuse_merge = decode_fuses_merge(pl.nsplit, static_cast<long long>(B) * Hkv, false) ? 1 : 0;
     make_rope_table(desc, &P.rope);
 
     CUtensorMap tm_k, tm_v;

@@ -216,7 +216,13 @@ spark_status spark_attn_prefill_chunk(const void *qkv, const float *gate, const 
  *   out      bf16 [B, H * 256]
  *   workspace >= spark_attn_decode_workspace_size(...) bytes (split-KV
  *            partial softmax states), 256-byte aligned, zeroed once before
- *            first use.
+ *            first use.  Its first 256 bytes are a header: the status word,
+ *            then counters of finished splits, one per (sequence, KV head),
+ *            used when a step has at most 8 splits per (sequence, KV head) and
+ *            B * Hkv <= 63 (the split kernel then also does the merge).
+ *            Every call leaves the counters at 0; do not write into the
+ *            header between calls (spark_attn_read_status clears only the
+ *            status word).
  * Returns 0 from the size query for invalid arguments.
  */
 size_t spark_attn_decode_workspace_size(int B, int H, int Hkv, int64_t cap,

@@ -261,3 +261,75 @@ def test_window_one_passes_v_through_bit_exact(cuda, H, Hkv):
     v = step["qkv"][:, (H + Hkv) * 256:].reshape(B, Hkv, 256)
     want = v[:, torch.arange(H) // G, :].reshape(B, H * 256)
     assert torch.equal(out.reshape(B, H * 256).cpu(), want)
+
+
+# Steps whose scans have 2..8 splits per (sequence, KV head): spark_attn_decode
+# merges them inside the split kernel, while spark_attn_decode_noalloc keeps the
+# separate merge kernel there (its scratch holds no split counters).  The two
+# merges run the same arithmetic in the same order.
+FUSED_CASES = [
+    # layer, H, Hkv, cap, positions (one per sequence)
+    (wl.SLIDING_LAYER, 16, 4, 512, [1048575]),                    # the 1M step's rings: 8 splits
+    (wl.SLIDING_LAYER, 16, 4, 512, [600, 511, 40]),               # one sequence with one split
+    (wl.FULL_LAYER, 16, 4, 300, [299, 0]),                        # nothing cached at pos 0
+    (wl.FULL_LAYER, 16, 2, 400, [399, 130]),                      # G = 8: two parts per head
+    (wl.SLIDING_LAYER, 8, 8, 512, [700, 300]),                    # G = 1
+    (wl.FULL_LAYER, 8, 4, 20000, [19999, 5000, 64, 1, 12345, 6000]),  # long chunks, 6 splits
+    (wl.Layer(kind=SLIDING, window=512, theta=1e4, rot_dim=256, gate_mode=1), 16, 4, 512,
+     [2000, 900]),                                                # silu gate
+]
+
+
+@pytest.mark.parametrize("layer,H,Hkv,cap,positions", FUSED_CASES)
+def test_merge_in_split_kernel_equals_merge_kernel(cuda, layer, H, Hkv, cap, positions):
+    B = len(positions)
+    g = torch.Generator(cuda).manual_seed(B * 131 + cap)
+    qkv = torch.randn((B, (H + 2 * Hkv) * 256), generator=g, device=cuda).to(torch.bfloat16)
+    gate = torch.randn((B, H), generator=g, device=cuda)
+    pos = torch.tensor(positions, dtype=torch.int32, device=cuda)
+    k = torch.randn((B, Hkv, cap, 256), generator=g, device=cuda).to(torch.bfloat16)
+    v = torch.randn((B, Hkv, cap, 256), generator=g, device=cuda).to(torch.bfloat16)
+    k2, v2 = k.clone(), v.clone()
+    ws = fga.new_workspace(fga.spark_attn_decode_workspace_size(B, H, Hkv, cap, layer))
+    fused = fga.spark_attn_decode(qkv, gate, pos, k, v, layer, workspace=ws)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda)
+    merged = fga.spark_attn_decode_noalloc(qkv, gate, pos, k2, v2, layer, device_status=status)
+    torch.cuda.synchronize()
+    assert fga.spark_attn_read_status(ws) == 0 and int(status.item()) == 0
+    assert torch.equal(fused, merged)
+    assert torch.equal(k, k2) and torch.equal(v, v2), "cache updates differ"
+    # the split counters (header words after the status word) are back at 0
+    assert int(torch.count_nonzero(ws[4:256])) == 0
+
+
+def test_split_counters_survive_repeated_and_mixed_calls(cuda):
+    """One workspace serves calls of different shapes in turn; each call finds
+    its counters at 0 and leaves them there, so every result stays right."""
+    layer = wl.SLIDING_LAYER
+    H, Hkv, cap = 16, 4, 512
+    size = max(fga.spark_attn_decode_workspace_size(B, H, Hkv, cap, layer) for B in (1, 2, 5))
+    ws = fga.new_workspace(size)
+    for i, B in enumerate((1, 5, 2, 1, 5)):
+        positions = [3000 + 97 * b + i for b in range(B)]
+        out = run_case_with_workspace(cuda, layer, H, Hkv, cap, positions, seed=40 + i, ws=ws)
+        del out
+        assert int(torch.count_nonzero(ws[4:256])) == 0
+
+
+def run_case_with_workspace(cuda, layer, H, Hkv, cap, positions, seed, ws):
+    B = len(positions)
+    case = wl.DecodeCase("t", B=B, H=H, Hkv=Hkv, layer=layer, seed=seed, cap=cap,
+                         len_lo=0, len_hi=0)
+    step = wl.make_decode_step_inputs(case)
+    pos = torch.tensor(positions, dtype=torch.int32)
+    kc = wl.fill_cache_(torch.empty((B, Hkv, cap, 256), dtype=torch.bfloat16), seed + 11)
+    vc = wl.fill_cache_(torch.empty_like(kc), seed + 12)
+    out = fga.spark_attn_decode(step["qkv"].to(cuda), step["gate"].to(cuda), pos.to(cuda),
+                                kc.to(cuda), vc.to(cuda), layer, workspace=ws)
+    torch.cuda.synchronize()
+    assert fga.spark_attn_read_status(ws) == 0
+    want, _, _ = oracle.decode(wl.bf16_bits(step["qkv"]), step["gate"].numpy(), pos.numpy(),
+                               wl.bf16_bits(kc), wl.bf16_bits(vc), layer.kind, layer.window,
+                               layer.theta, layer.rot_dim, H, Hkv)
+    check_close(out, want, f"decode B={B} pos={positions} (shared workspace)")
+    return out
