@@ -333,3 +333,17 @@ def run_case_with_workspace(cuda, layer, H, Hkv, cap, positions, seed, ws):
                                layer.theta, layer.rot_dim, H, Hkv)
     check_close(out, want, f"decode B={B} pos={positions} (shared workspace)")
     return out
+
+
+@pytest.mark.parametrize("B,H,Hkv", [(21, 12, 3), (16, 16, 4)], ids=["63-counters", "64-pairs"])
+def test_split_counter_capacity(cuda, B, H, Hkv):
+    """The workspace header holds 63 split counters.  With B * Hkv = 63 pairs
+    the last header word is used; with 64 the merge kernel runs instead.
+    Both give the oracle's result and leave the header words at 0."""
+    layer = wl.SLIDING_LAYER
+    cap = 512
+    ws = fga.new_workspace(fga.spark_attn_decode_workspace_size(B, H, Hkv, cap, layer))
+    for rep in range(2):
+        positions = [600 + 37 * b + rep for b in range(B)]
+        run_case_with_workspace(cuda, layer, H, Hkv, cap, positions, seed=60 + rep, ws=ws)
+        assert int(torch.count_nonzero(ws[4:256])) == 0
