@@ -38,8 +38,12 @@ constexpr int kDecThreads = (kDecWarps + 1) * 32;         // + one producer warp
 constexpr int kDecTileBytes = kDecTile * kHeadDim * 2;    // 32 KB (K or V)
 constexpr int kDecStageBytes = 2 * kDecTileBytes;         // K + V
 constexpr int kDecQBytes = 8 * kHeadDim * 2;              // 8 (padded) query heads
-constexpr int dec_smem_bytes(int stages) {
-    return 1024 + stages * kDecStageBytes + kDecQBytes + 2 * stages * 8;
+// Kernels that merge: the new token's rotated key and value, and the gate
+// logits of the group's (at most 8) heads.
+constexpr int kDecNewBytes = 2 * kHeadDim * 2 + 8 * 4;
+constexpr int dec_smem_bytes(int stages, bool fuse) {
+    return 1024 + stages * kDecStageBytes + kDecQBytes + (fuse ? kDecNewBytes : 0) +
+           2 * stages * 8;
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
@@ -131,12 +135,44 @@ __device__ __forceinline__ NewToken score_new_token(const DecodeParams &P, int b
     return nt;
 }
 
+// The same NewToken from shared memory, where the split kernel's prologue put
+// q and the new key rotated and rounded to bf16 (the same values
+// score_new_token computes) and the new value: one dot product, no loads from
+// global memory.
+__device__ __forceinline__ NewToken new_token_from_smem(const __nv_bfloat16 *qs,
+                                                        const __nv_bfloat16 *kn,
+                                                        const __nv_bfloat16 *vn, int hq,
+                                                        int lane) {
+    NewToken nt;
+    const uint4 qv = *reinterpret_cast<const uint4 *>(qs + hq * kHeadDim + lane * 8);
+    const uint4 kv = *reinterpret_cast<const uint4 *>(kn + lane * 8);
+    nt.vv = *reinterpret_cast<const uint4 *>(vn + lane * 8);
+    const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+    const uint32_t vw[4] = {nt.vv.x, nt.vv.y, nt.vv.z, nt.vv.w};
+    nt.kb[0] = kv.x;
+    nt.kb[1] = kv.y;
+    nt.kb[2] = kv.z;
+    nt.kb[3] = kv.w;
+    float dot = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        nt.v[2 * i] = bf16_lo(vw[i]);
+        nt.v[2 * i + 1] = bf16_hi(vw[i]);
+        dot = fmaf(bf16_lo(qw[i]), bf16_lo(nt.kb[i]), dot);
+        dot = fmaf(bf16_hi(qw[i]), bf16_hi(nt.kb[i]), dot);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+    nt.x_new = dot * kScaleLog2;
+    return nt;
+}
+
 // Gated output of head h and, for the first head of the group, the new
 // key/value stored at slot(pos) (write-then-attend: no split reads that slot).
 __device__ __forceinline__ void store_head(const DecodeParams &P, int b, int g, int hq, int h,
                                            long long p, int d0, const float (&acc)[8], float L,
-                                           const NewToken &nt) {
-    const float scale = gate_act(P.gate[static_cast<size_t>(b) * P.H + h], P.gate_mode) / L;
+                                           const NewToken &nt, float gate_logit) {
+    const float scale = gate_act(gate_logit, P.gate_mode) / L;
     uint4 ov;
     ov.x = pack_bf16x2(acc[0] * scale, acc[1] * scale);
     ov.y = pack_bf16x2(acc[2] * scale, acc[3] * scale);
@@ -204,7 +240,7 @@ __device__ __forceinline__ void merge_parts(const NewToken &nt, float M, int nva
 // them, so they are read at L2 (ld.global.cg).
 __device__ __forceinline__ void merge_head_in_split(const DecodeParams &P, int b, int g, int hq,
                                                     long long p, int nvalid, int lane,
-                                                    const NewToken &nt) {
+                                                    const NewToken &nt, float gate_logit) {
     const int h = g * P.G + hq, d0 = lane * 8;
     const size_t part0 = (static_cast<size_t>(b) * P.H + h) * P.nsplit;
     float2 ml[kFuseMaxSplits];
@@ -230,7 +266,7 @@ __device__ __forceinline__ void merge_head_in_split(const DecodeParams &P, int b
         merge_parts<kMergeWarps>(nt, M, nvalid, ml, pa, pc, acc, L);
     else
         merge_parts<2>(nt, M, nvalid, ml, pa, pc, acc, L);
-    store_head(P, b, g, hq, h, p, d0, acc, L, nt);
+    store_head(P, b, g, hq, h, p, d0, acc, L, nt, gate_logit);
 }
 
 // kFuse: this CTA's grid merges itself (P.fuse_merge); a separate
@@ -245,7 +281,12 @@ __global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *stages = smem;
     __nv_bfloat16 *qs = reinterpret_cast<__nv_bfloat16 *>(smem + kDecStages * kDecStageBytes);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kDecStages * kDecStageBytes + kDecQBytes);
+    // (kernels that merge) the new token's key, rotated, its value and the gates
+    __nv_bfloat16 *kn = qs + 8 * kHeadDim;
+    __nv_bfloat16 *vn = kn + kHeadDim;
+    float *gq = reinterpret_cast<float *>(vn + kHeadDim);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kDecStages * kDecStageBytes + kDecQBytes +
+                                                  (kFuse ? kDecNewBytes : 0));
     uint64_t *empty = full + kDecStages;
     __shared__ int abort_flag;
     __shared__ float red_m[kDecWarps][8];
@@ -271,7 +312,8 @@ __global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
         if (kFuse && n_scan == 0 && split == 0 && warp < kDecWarps)
             for (int hq = warp; hq < P.G; hq += kDecWarps)
                 merge_head_in_split(P, b, g, hq, p, 0, lane,
-                                    score_new_token(P, b, g, g * P.G + hq, p, lane));
+                                    score_new_token(P, b, g, g * P.G + hq, p, lane),
+                                    P.gate[static_cast<size_t>(b) * P.H + g * P.G + hq]);
         return;
     }
     const int ntiles = static_cast<int>((c_hi - c_lo + kDecTile - 1) / kDecTile);
@@ -315,6 +357,18 @@ __global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
                 P.qkv + b * width + static_cast<size_t>(g * P.G + hh) * kHeadDim + v * 8);
         *reinterpret_cast<uint4 *>(qs + hh * kHeadDim + v * 8) = val;
     }
+    if constexpr (kFuse) {
+        // the new token for the merge at the end, loaded with q
+        if (tid < 2 * (kHeadDim / 8)) {
+            const int which = tid / (kHeadDim / 8), v = tid % (kHeadDim / 8);
+            const uint4 val = *reinterpret_cast<const uint4 *>(
+                P.qkv + b * width + static_cast<size_t>(P.H + which * P.Hkv + g) * kHeadDim + v * 8);
+            *reinterpret_cast<uint4 *>((which ? vn : kn) + v * 8) = val;
+        } else if (tid < 2 * (kHeadDim / 8) + P.G) {
+            const int hh = tid - 2 * (kHeadDim / 8);
+            gq[hh] = P.gate[static_cast<size_t>(b) * P.H + g * P.G + hh];
+        }
+    }
     __syncthreads();
     const int half = P.rope.rot_dim / 2;
     for (int k = tid; k < half; k += kDecThreads) {
@@ -327,6 +381,14 @@ __global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
             rope_rotate(x1, x2, c, s, y1, y2);
             qs[hh * kHeadDim + k] = __float2bfloat16_rn(y1);
             qs[hh * kHeadDim + k + half] = __float2bfloat16_rn(y2);
+        }
+        if constexpr (kFuse) {
+            const float x1 = __bfloat162float(kn[k]);
+            const float x2 = __bfloat162float(kn[k + half]);
+            float y1, y2;
+            rope_rotate(x1, x2, c, s, y1, y2);
+            kn[k] = __float2bfloat16_rn(y1);
+            kn[k + half] = __float2bfloat16_rn(y2);
         }
     }
     __syncthreads();
@@ -533,13 +595,13 @@ __global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
     // aborted one too, so the count always completes and returns to 0); the
     // one that completes the count merges.  No thread waits on another CTA.
     const int nvalid = static_cast<int>((n_scan + P.chunk - 1) / P.chunk);
-    // The new token of this warp's heads (warp, warp + 4) first: its loads
-    // then overlap the count instead of following it.
+    // The new token of this warp's heads (warp, warp + 4), from the copy the
+    // prologue staged in shared memory.
     NewToken nt[2];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         const int hq = warp + i * kDecWarps;
-        if (hq < P.G) nt[i] = score_new_token(P, b, g, g * P.G + hq, p, lane);
+        if (hq < P.G) nt[i] = new_token_from_smem(qs, kn, vn, hq, lane);
     }
     if (nvalid > 1) {
         __shared__ int last_cta;
@@ -557,7 +619,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         const int hq = warp + i * kDecWarps;
-        if (hq < P.G) merge_head_in_split(P, b, g, hq, p, nvalid, lane, nt[i]);
+        if (hq < P.G) merge_head_in_split(P, b, g, hq, p, nvalid, lane, nt[i], gq[hq]);
     }
 }
 
@@ -637,7 +699,7 @@ __global__ void __launch_bounds__(512) decode_merge_kernel(const __grid_constant
         acc[7] += c.w;
         L += red_l[hq][w];
     }
-    store_head(P, b, g, hq, h, p, d0, acc, L, nt);
+    store_head(P, b, g, hq, h, p, d0, acc, L, nt, P.gate[static_cast<size_t>(b) * P.H + h]);
 }
 
 // ---------------------------------------------------------------- launchers
@@ -649,7 +711,7 @@ cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, cons
                                              : decode_split_kernel<1, false>)
                              : (P.fuse_merge ? decode_split_kernel<kDecStagesLong, true>
                                              : decode_split_kernel<kDecStagesLong, false>);
-    const int smem = dec_smem_bytes(short_scan ? 1 : kDecStagesLong);
+    const int smem = dec_smem_bytes(short_scan ? 1 : kDecStagesLong, P.fuse_merge != 0);
     cudaError_t err =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
