@@ -5,7 +5,7 @@
 // the Spark-X2.5-4B hybrid-attention explainer (lshu.cn) describes: full
 // layers keep every token, sliding layers only the latest `window`.
 //
-// Two kernels on one stream:
+// One or two kernels on one stream:
 //   decode_split_kernel  grid (nsplit, Hkv, B).  Each CTA streams a chunk of
 //       cache slots of one (sequence, KV head) through a TMA ring in shared
 //       memory and keeps an online softmax for the G query heads of the group
@@ -15,10 +15,11 @@
 //   decode_merge_kernel  grid (Hkv, B).  Rotates q and the new key, scores the
 //       new token, merges it with the partial states (log-sum-exp rescale),
 //       applies the gate, and stores the new key/value at slot(pos).
-// When a (sequence, KV head) has at most kFuseMaxSplits splits (rings, short
-// caches) the split kernel does the merge itself, with the same arithmetic:
-// the CTA that finishes last (a counter of finished splits in the workspace)
-// merges the states, so the step is one launch instead of two.
+// When each (sequence, KV head) has one split, or at most kFuseMaxSplits of
+// them and B * Hkv fits the counters of the workspace header (rings, short
+// caches), the split kernel does the merge itself, with the same arithmetic:
+// the CTA that finishes last (a counter of finished splits) merges the
+// states, so the step is one launch instead of two.
 // The new token is not read from the cache by the split kernel, so the cache
 // write can come last without a race: on a full layer slot(pos) lies past
 // every cached token, and on a ring it holds token pos - cap, which is out of
