@@ -114,6 +114,14 @@ def decode_kv_bytes(layers) -> tuple[int, int]:
     return total, full
 
 
+def decode_step_launches(dec) -> int:
+    """Kernels one decode step enqueues, as the library reports them: per layer
+    1 (the split kernel merges itself) or 2 (split kernel, then merge kernel)."""
+    import full_gqa_attention_gb300 as fga
+    return sum(fga.spark_attn_decode_launch_count(L["case"].B, L["case"].H, L["case"].Hkv,
+                                                  L["case"].cap, L["layer"]) for L in dec)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -387,7 +395,7 @@ def run_ours(args, rank, world, local):
     e2e_prefill_max = dist_max(e2e_prefill_ms, world)
     e2e_decode_max = dist_max(e2e_decode_ms, world)
     status = int(dist_max(float(status), world))
-    launches = args.steps * ((2 if pre is not None else 0) + 2 * len(dec))
+    launches = args.steps * ((2 if pre is not None else 0) + decode_step_launches(dec))
     launches_all = int(dist_sum(float(launches), world))
     if rank != 0:
         return None

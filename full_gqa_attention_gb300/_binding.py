@@ -64,6 +64,8 @@ def _load() -> ctypes.CDLL:
     lib.spark_attn_prefill_chunk.restype = i32
     lib.spark_attn_decode_workspace_size.argtypes = [i32, i32, i32, i64, D]
     lib.spark_attn_decode_workspace_size.restype = sz
+    lib.spark_attn_decode_launch_count.argtypes = [i32, i32, i32, i64, D]
+    lib.spark_attn_decode_launch_count.restype = i32
     lib.spark_attn_decode.argtypes = [P, P, P, P, P, i64, D, i32, i32, i32, P, P, sz, P]
     lib.spark_attn_decode.restype = i32
     lib.spark_attn_decode_noalloc.argtypes = [P, P, P, P, P, i64, D, i32, i32, i32, P, P, P]
@@ -174,6 +176,12 @@ def spark_attn_prefill_workspace_size(B: int, T: int, H: int, Hkv: int, layer) -
 def spark_attn_decode_workspace_size(B: int, H: int, Hkv: int, cap: int, layer) -> int:
     d = as_desc(layer)
     return lib.spark_attn_decode_workspace_size(B, H, Hkv, cap, ctypes.byref(d))
+
+
+def spark_attn_decode_launch_count(B: int, H: int, Hkv: int, cap: int, layer) -> int:
+    """Kernels one spark_attn_decode call enqueues (1 or 2; 0 if invalid)."""
+    d = as_desc(layer)
+    return lib.spark_attn_decode_launch_count(B, H, Hkv, cap, ctypes.byref(d))
 
 
 def new_workspace(nbytes: int, device=None) -> torch.Tensor:

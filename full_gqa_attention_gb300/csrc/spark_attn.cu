@@ -432,6 +432,13 @@ size_t spark_attn_decode_workspace_size(int B, int H, int Hkv, int64_t cap,
     return plan_decode(B, H, Hkv, cap, desc, sm_count_or_default()).bytes;
 }
 
+int spark_attn_decode_launch_count(int B, int H, int Hkv, int64_t cap,
+                                   const spark_layer_desc *desc) {
+    if (check_decode(B, H, Hkv, cap, desc) != SPARK_OK || B == 0) return 0;
+    const DecodePlan pl = plan_decode(B, H, Hkv, cap, desc, sm_count_or_default());
+    return decode_fuses_merge(pl.nsplit, static_cast<long long>(B) * Hkv, true) ? 1 : 2;
+}
+
 spark_status spark_attn_decode(const void *qkv, const float *gate, const int32_t *pos,
                                void *k_cache, void *v_cache, int64_t cap,
                                const spark_layer_desc *desc, int B, int H, int Hkv, void *out,

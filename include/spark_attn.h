@@ -235,6 +235,17 @@ spark_status spark_attn_decode(const void *qkv, const float *gate, const int32_t
                                void *stream);
 
 /*
+ * Number of kernels one spark_attn_decode call with these arguments enqueues
+ * on the current device: 2 (the split kernel, then the merge kernel) or 1
+ * (the split kernel merges itself: one split per (sequence, KV head), or at
+ * most 8 of them with B * Hkv <= 63).  For callers that count or budget
+ * launches (CUDA graphs, schedulers).  Returns 0 for invalid arguments and
+ * for B == 0.  Host-only: touches no device memory.
+ */
+int spark_attn_decode_launch_count(int B, int H, int Hkv, int64_t cap,
+                                   const spark_layer_desc *desc);
+
+/*
  * Decode without a caller-provided workspace.
  *
  * The paper has no counterpart to this call; it exists for callers that

@@ -167,3 +167,20 @@ def test_layer_calls_check_before_enqueueing():
     assert L.spark_attn_layer_prefill_workspace_size(2, 8192, 2561, 16, 4, d) == 0
     assert L.spark_attn_layer_decode_workspace_size(1, 2560, 16, 4, 1 << 20, d) > \
         L.spark_attn_decode_workspace_size(1, 16, 4, 1 << 20, d)
+
+
+def test_decode_launch_count():
+    """1 launch where the split kernel merges itself, 2 where the merge kernel
+    follows it, 0 for invalid arguments or an empty batch (plan for the
+    152-SM GB300 when no device is visible)."""
+    full = desc(kind=0, window=0, theta=5e6, rot=64)
+    ring = desc()
+    count = fga.lib.spark_attn_decode_launch_count
+    assert count(1, 16, 4, 512, ctypes.byref(ring)) == 1          # 8 splits, 4 counters
+    assert count(64, 16, 4, 512, ctypes.byref(ring)) == 1         # one split each
+    assert count(1, 16, 4, 1 << 20, ctypes.byref(full)) == 2      # 38 splits
+    assert count(21, 12, 3, 512, ctypes.byref(ring)) == 1         # 63 counters: the last word
+    assert count(16, 16, 4, 512, ctypes.byref(ring)) == 2         # 64 pairs, 2 splits each
+    assert count(0, 16, 4, 512, ctypes.byref(ring)) == 0
+    assert count(1, 16, 5, 512, ctypes.byref(ring)) == 0          # H % Hkv != 0
+    assert count(1, 16, 4, 512, None) == 0

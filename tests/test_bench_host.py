@@ -58,3 +58,11 @@ def test_pack_decode_io_outputs_do_not_overlap(monkeypatch):
         L["out"].fill_(float(i + 1))
     for i, L in enumerate(dec):
         assert torch.all(L["out"] == float(i + 1))
+
+
+def test_decode_step_launch_count_of_the_1m_step():
+    """The 1M-context step: 9 full layers (38 splits each: split + merge kernel)
+    and 27 rings (8 splits, B * Hkv = 4: the split kernel merges itself)."""
+    dec = [{"case": bench.DECODE_FULL if layer.kind == bench.wl.FULL else bench.DECODE_SLIDING,
+            "layer": layer} for layer in bench.decode_layers(36)]
+    assert bench.decode_step_launches(dec) == 9 * 2 + 27 * 1
