@@ -185,7 +185,8 @@ def spark_attn_decode_launch_count(B: int, H: int, Hkv: int, cap: int, layer) ->
 
 
 def new_workspace(nbytes: int, device=None) -> torch.Tensor:
-    """A zeroed workspace (the status word must start at 0)."""
+    """A zeroed workspace: the header's status word and decode split counters
+    must start at 0 (every call leaves the counters at 0 again)."""
     return torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device or "cuda")
 
 
