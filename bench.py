@@ -174,24 +174,36 @@ def dist_sum(x: float, world: int) -> float:
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples while the timed region runs."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock / throttle samples while the timed region runs.
+
+    Each sample carries nvidia-smi's timestamp, so that the samples taken
+    inside the timed region (between mark_start and mark_end) are told apart
+    from those of the untimed repeat of the same step that follows it."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 100
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
+        self.t_start = self.t_end = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
         return self
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
 
     def __exit__(self, *exc):
         self.lines = []
@@ -205,25 +217,46 @@ class ClockSampler:
             self.lines = [l for l in out.splitlines() if l.strip()]
         return False
 
+    @staticmethod
+    def _when(stamp: str):
+        import datetime
+        try:
+            return datetime.datetime.strptime(stamp, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
     def summary(self):
-        sm, mx, reasons = [], [], set()
+        sm, mx, reasons, in_timed = [], [], set(), 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for l in getattr(self, "lines", []):
             f = [x.strip() for x in l.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
+                sm.append(float(f[2]))
+                mx.append(float(f[3]))
             except ValueError:
                 continue
-            for name, v in zip(names, f[5:9]):
+            t = self._when(f[0])
+            if (t is not None and self.t_start is not None and self.t_end is not None
+                    and self.t_start <= t <= self.t_end):
+                in_timed += 1
+            for name, v in zip(names, f[6:10]):
                 if v.lower() == "active":
                     reasons.add(name)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "sm_mhz_min": min(sm), "reasons": sorted(reasons), "samples": len(sm),
+                "samples_in_timed_region": in_timed, "interval_ms": self.INTERVAL_MS,
+                "window": "the timed steps, then the same step repeated untimed for "
+                          f"{CLOCK_SOAK_S:.1f} s so that the load is sampled often enough"}
+
+
+# After the timed steps the same step runs on, untimed, this long while the
+# clock sampler keeps going: the timed region alone is too short for the
+# sampler's interval.
+CLOCK_SOAK_S = 2.5
 
 
 # ---------------------------------------------------------------- our arm
@@ -312,12 +345,20 @@ def run_ours(args, rank, world, local):
     with ClockSampler(local) as clocks:
         dist_barrier(world)
         torch.cuda.synchronize()
+        clocks.mark_start()
         start.record(stream)
         for _ in range(args.steps):
             step(timing)
         stop.record(stream)
         torch.cuda.synchronize()
+        clocks.mark_end()
         dist_barrier(world)
+        # the same load, untimed, while the sampler keeps sampling
+        t_soak = time.time() + CLOCK_SOAK_S
+        while time.time() < t_soak:
+            for _ in range(4):
+                step()
+            torch.cuda.synchronize()
     total_ms = start.elapsed_time(stop) / args.steps
 
     def mean_ms(a, b):
@@ -494,7 +535,7 @@ def run_ours(args, rank, world, local):
     if pre is not None and dec and rank == 0 and not args.no_other_configs:
         line["other_configs"] = time_other_configs(fga, dev, bf16_peak, hbm_peak)
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args)
+        line["cpu_baseline"] = cpu_baseline(args, dec)
     return line
 
 
@@ -764,25 +805,154 @@ TRAFFIC: dict[str, float | None] = {
 _ORACLE_INPUTS = {}
 
 
-def oracle_prefill_sample(n_rows: int, seed: int = 0):
-    """Times the fp64 oracle on n_rows query rows of the prefill workload.
-    Returns (seconds, algorithmic flops of those rows, description)."""
+def _prefill_inputs(case):
+    if case.name not in _ORACLE_INPUTS:
+        x = wl.make_prefill_inputs(case)
+        _ORACLE_INPUTS[case.name] = (x, wl.bf16_bits(x["qkv"]))
+    return _ORACLE_INPUTS[case.name]
+
+
+def _visible(t, case):
+    """Visible keys of query rows at token indices t (mask definition)."""
+    import numpy as np
+    t = np.asarray(t, np.int64)
+    if case.layer.kind == wl.FULL:
+        return t + 1
+    return np.minimum(t + 1, case.layer.window)
+
+
+def oracle_prefill_rows(case, n_rows: int, seed: int = 0):
+    """Times the fp64 oracle on n_rows random query rows (all heads) of a
+    prefill workload, or on all of it when n_rows >= B*T.  Returns (seconds,
+    algorithmic flops of those rows, fraction of the workload's flops,
+    description)."""
     import numpy as np
     import oracle
-    c = PREFILL
-    if not _ORACLE_INPUTS:
-        x = wl.make_prefill_inputs(c)
-        _ORACLE_INPUTS.update(x=x, bits=wl.bf16_bits(x["qkv"]))
-    x, bits = _ORACLE_INPUTS["x"], _ORACLE_INPUTS["bits"]
-    rng = np.random.default_rng(seed)
-    rows = np.sort(rng.integers(0, c.B * c.T, n_rows)).astype(np.int64)
-    L = c.layer
+    x, bits = _prefill_inputs(case)
+    total_rows = case.B * case.T
+    L = case.layer
+    if n_rows >= total_rows:
+        rows = None
+        vis = _visible(np.arange(case.T), case).sum() * case.B
+        desc = f"the whole {case.name} workload ({total_rows} query rows)"
+    else:
+        rng = np.random.default_rng(seed)
+        rows = np.sort(rng.integers(0, total_rows, n_rows)).astype(np.int64)
+        vis = _visible(rows % case.T, case).sum()
+        desc = f"{n_rows} random query rows (all {case.H} heads) of {case.name}"
     t0 = time.perf_counter()
     oracle.prefill(bits, x["gate"].numpy(), x["pos"].numpy(), L.kind, L.window, L.theta,
-                   L.rot_dim, c.H, c.Hkv, rows=rows)
+                   L.rot_dim, case.H, case.Hkv, rows=rows, gate_mode=L.gate_mode)
     dt = time.perf_counter() - t0
-    flops = 4.0 * 256 * c.H * float(np.sum(rows % c.T + 1))
-    return dt, flops, f"{n_rows} random query rows (all 16 heads) of the B=2 T=8192 prefill"
+    flops = 4.0 * 256 * case.H * float(vis)
+    return dt, flops, flops / prefill_flops(case), desc
+
+
+def oracle_prefill_sample(n_rows: int, seed: int = 0):
+    """The oracle on n_rows random query rows of the benchmark's prefill."""
+    dt, flops, _, desc = oracle_prefill_rows(PREFILL, n_rows, seed)
+    return dt, flops, desc
+
+
+def _sized(run, target_s: float, n0: int, n_max: int):
+    """Calls run(n) with n growing from n0 until one call takes >= target_s
+    seconds or n reaches n_max; returns the last call's result (time first)."""
+    n = n0
+    while True:
+        res = run(n)
+        if res[0] >= target_s or n >= n_max:
+            return res
+        n = min(n_max, int(n * min(8.0, max(2.0, 1.5 * target_s / max(res[0], 1e-3)))))
+
+
+def oracle_decode_time(case, positions, k_bits, v_bits):
+    """Seconds the fp64 oracle takes for one decode step of the given
+    sequences (qkv / gate from the workload's seeded step inputs)."""
+    import numpy as np
+    import oracle
+    step = wl.make_decode_step_inputs(wl.scaled(case, B=len(positions)))
+    L = case.layer
+    pos = np.asarray(positions, np.int32)
+    t0 = time.perf_counter()
+    oracle.decode(wl.bf16_bits(step["qkv"]), step["gate"].numpy(), pos, k_bits, v_bits, L.kind,
+                  L.window, L.theta, L.rot_dim, case.H, case.Hkv, gate_mode=L.gate_mode)
+    return time.perf_counter() - t0
+
+
+def _cpu_cache(B, Hkv, n, seed):
+    """A seeded bf16 cache [B, Hkv, n, 256] on the host, as bit patterns."""
+    import torch
+    c = torch.empty((B, Hkv, n, 256), dtype=torch.bfloat16)
+    g = torch.Generator().manual_seed(seed)
+    for b in range(B):
+        c[b].copy_(torch.randn((Hkv, n, 256), generator=g).to(torch.bfloat16))
+    return wl.bf16_bits(c)
+
+
+def oracle_decode_batched(case, n_seq: int, seed: int = 0):
+    """The oracle on n_seq of the batched decode workload's sequences (all 64
+    when n_seq >= B), each at its own length, caches seeded on the host.
+    Returns (seconds, KV bytes read, fraction of the workload's KV bytes,
+    description)."""
+    import numpy as np
+    lengths = wl.make_decode_lengths(case).numpy().astype(np.int64)
+    if n_seq >= case.B:
+        seqs = np.arange(case.B)
+    else:
+        seqs = np.sort(np.random.default_rng(seed).choice(case.B, n_seq, replace=False))
+    visible = lambda p: (p + 1) if case.layer.kind == wl.FULL else min(p + 1, case.layer.window)  # noqa: E731
+    dt, kv = 0.0, 0
+    if case.layer.kind == wl.SLIDING:
+        # rings: every sequence in one oracle call
+        pos = lengths[seqs]
+        k = _cpu_cache(len(seqs), case.Hkv, case.cap, seed + 1)
+        v = _cpu_cache(len(seqs), case.Hkv, case.cap, seed + 2)
+        dt = oracle_decode_time(case, pos, k, v)
+        kv = sum(visible(int(p)) for p in pos) * KV_BYTES_PER_TOKEN
+    else:
+        for i, b in enumerate(seqs):
+            p = int(lengths[b])
+            k = _cpu_cache(1, case.Hkv, p + 1, seed + 3 * i + 1)
+            v = _cpu_cache(1, case.Hkv, p + 1, seed + 3 * i + 2)
+            dt += oracle_decode_time(case, [p], k, v)
+            kv += visible(p) * KV_BYTES_PER_TOKEN
+            del k, v
+    total = sum(visible(int(p)) for p in lengths) * KV_BYTES_PER_TOKEN
+    what = "all" if len(seqs) == case.B else f"{len(seqs)} seeded-random"
+    return dt, kv, kv / total, f"{what} of the {case.B} sequences of {case.name}"
+
+
+def oracle_decode_1m(dec):
+    """The oracle on one full layer (1,048,575 cached tokens, the cache read
+    back from the benchmark's own device copy) and one sliding layer of the
+    1M-context decode step; the 36-layer step is extrapolated as 9 full + 27
+    sliding layers.  Returns (step seconds extrapolated, KV bytes of the
+    step, seconds measured, description)."""
+    full = next((L for L in dec if L["layer"].kind == wl.FULL), None)
+    slid = next((L for L in dec if L["layer"].kind == wl.SLIDING), None)
+    n_full = sum(1 for L in dec if L["layer"].kind == wl.FULL)
+    n_slid = len(dec) - n_full
+    measured, t_full, t_slid = 0.0, 0.0, 0.0
+    for L, kind in ((full, "full"), (slid, "sliding")):
+        if L is None:
+            continue
+        c = L["case"]
+        p = int(L["host"]["pos"][0])
+        n = min(p + 1, c.cap) if kind == "full" else c.cap
+        k = wl.bf16_bits(L["k"][:, :, :n].cpu())
+        v = wl.bf16_bits(L["v"][:, :, :n].cpu())
+        t = oracle_decode_time(c, [p], k, v)
+        del k, v
+        measured += t
+        if kind == "full":
+            t_full = t
+        else:
+            t_slid = t
+    step_s = n_full * t_full + n_slid * t_slid
+    kv, _ = decode_kv_bytes([L["layer"] for L in dec])
+    return step_s, kv, measured, (f"one full layer (1,048,575 cached tokens) and one sliding "
+                                  f"layer, extrapolated to the {n_full} + {n_slid} layers of "
+                                  "the step")
 
 
 def cpu_threads() -> int:
@@ -796,16 +966,49 @@ def cpu_threads() -> int:
         return os.cpu_count() or 1
 
 
-def cpu_baseline(args):
-    """The fp64 oracle, as it stands, on a bounded sample (~10-30 s of CPU)."""
-    n = 64
-    while True:
-        dt, flops, desc = oracle_prefill_sample(n)
-        if dt >= 8.0 or n >= 8192:
-            break
-        n = int(n * min(8.0, max(2.0, 10.0 / max(dt, 1e-3))))
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(),
-            "kind": "oracle", "sample": desc + f", {dt:.1f} s"}
+def cpu_baseline(args, dec=None):
+    """The fp64 oracle, as it stands, on host cores, beside every workload the
+    line reports: bounded samples (~25 s of CPU in all), each extrapolated to
+    its whole workload where it is a sample.  The headline entry is the
+    benchmark's prefill; per_config holds one entry per workload."""
+    cores = cpu_threads()
+    per = {}
+
+    def prefill_entry(case, target_s, n0):
+        total_rows = case.B * case.T
+        if target_s is None:
+            dt, flops, frac, desc = oracle_prefill_rows(case, total_rows)
+        else:
+            dt, flops, frac, desc = _sized(lambda n: oracle_prefill_rows(case, n), target_s,
+                                           n0, total_rows)
+        e = {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+             "sample": desc + f", {dt:.2f} s", "seconds": dt}
+        if frac < 1.0:
+            e["workload_seconds_extrapolated"] = dt / frac
+        return e
+
+    per["small_prefill_1.7b_sliding_T1024"] = prefill_entry(wl.PREFILL_SLIDING_1P7B_T1024,
+                                                            None, 0)
+    per["prefill_4b_full_B2_T8192"] = prefill_entry(PREFILL, 5.0, 64)
+    per["long_prefill_full_T65536"] = prefill_entry(wl.PREFILL_FULL_4B_T65536, 3.0, 16)
+    per["long_prefill_sliding_T65536"] = prefill_entry(wl.PREFILL_SLIDING_4B_T65536, 3.0, 256)
+    for key, case, n in (("batched_decode_full_B64", wl.DECODE_FULL_4B_B64, 8),
+                         ("batched_decode_sliding_B64", wl.DECODE_SLIDING_4B_B64, 64)):
+        dt, kv, frac, desc = oracle_decode_batched(case, n)
+        e = {"value": kv / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+             "sample": desc + f", {dt:.2f} s", "seconds": dt}
+        if frac < 1.0:
+            e["workload_seconds_extrapolated"] = dt / frac
+        per[key] = e
+    if dec:
+        step_s, kv, measured, desc = oracle_decode_1m(dec)
+        per["decode_step_1m_36_layers"] = {
+            "value": kv / step_s / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": desc + f", {measured:.2f} s measured", "seconds": measured,
+            "workload_seconds_extrapolated": step_s}
+    head = per["prefill_4b_full_B2_T8192"]
+    return {"value": head["value"], "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": head["sample"], "per_config": per}
 
 
 def run_reference(args, rank, world):

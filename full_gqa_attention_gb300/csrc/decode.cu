@@ -584,6 +584,18 @@ __global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
             *reinterpret_cast<float2 *>(P.part_ml + 2 * (part0 + static_cast<size_t>(hh) * P.nsplit +
                                                          split)) = ml;
         }
+    } else {
+        // A wait gave up (the status word says so): leave a neutral state
+        // (max -inf, sum 0, output 0), which the merge weighs by 0, so that
+        // it never merges what an earlier call left in a shared buffer.
+        const size_t part0 = (static_cast<size_t>(b) * P.H + static_cast<size_t>(g) * P.G) * P.nsplit;
+        for (int i = tid; i < P.G * kHeadDim; i += kDecWarps * 32) {
+            const int hh = i / kHeadDim, d = i % kHeadDim;
+            P.part_o[(part0 + static_cast<size_t>(hh) * P.nsplit + split) * kHeadDim + d] = 0.f;
+        }
+        if (tid < P.G)
+            *reinterpret_cast<float2 *>(P.part_ml + 2 * (part0 + static_cast<size_t>(tid) * P.nsplit +
+                                                         split)) = make_float2(-INFINITY, 0.f);
     }
     if constexpr (!kFuse) {
         __syncthreads();

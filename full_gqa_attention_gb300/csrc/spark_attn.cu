@@ -535,10 +535,43 @@ constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // SPARK_NOALLOC_SCRAT
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 std::mutex g_noalloc_mutex;
-void *g_noalloc_ptr[64] = {};
 
-// Device address of the scratch buffer on the current device, looked up once
-// per device (with that device current).  Returns nullptr on failure.
+// The buffer's device address per device, with the context it was looked up
+// in: a device reset rebuilds the primary context and reloads the module, so
+// an address is reused only while the same context is current.
+struct NoAllocAddr {
+    CUcontext ctx = nullptr;
+    void *ptr = nullptr;
+};
+NoAllocAddr g_noalloc_addr[64];
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+
+CtxGetCurrentFn ctx_get_current_fn() {
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+CUcontext current_context() {
+    CtxGetCurrentFn fn = ctx_get_current_fn();
+    CUcontext ctx = nullptr;
+    if (!fn || fn(&ctx) != CUDA_SUCCESS) return nullptr;
+    return ctx;
+}
+
+// Device address of the scratch buffer on the current device, looked up with
+// that device current: once per device, and again whenever another context is
+// current than the one of the last lookup.  Returns nullptr on failure.
 void *noalloc_scratch() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
@@ -546,15 +579,18 @@ void *noalloc_scratch() {
         return nullptr;
     }
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
-            cudaGetLastError();
-            return nullptr;
-        }
-        g_noalloc_ptr[dev] = p;
+    NoAllocAddr &a = g_noalloc_addr[dev];
+    if (a.ptr && a.ctx != nullptr && a.ctx == current_context()) return a.ptr;
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+        cudaGetLastError();
+        a = NoAllocAddr();
+        return nullptr;
     }
-    return g_noalloc_ptr[dev];
+    // the lookup made the device's context current if it was not yet
+    a.ctx = current_context();
+    a.ptr = p;
+    return p;
 }
 
 }  // namespace

@@ -269,10 +269,17 @@ int spark_attn_decode_launch_count(int B, int H, int Hkv, int64_t cap,
  *    results; order them on one stream.
  *  - Set-up: the first call on each device looks up the buffer's device
  *    address (cudaGetSymbolAddress, with that device current).  Make that
- *    first call before any stream capture.
+ *    first call before any stream capture.  The address is kept per device
+ *    together with the CUDA context it belongs to; when a later call finds
+ *    another context current on the device (the caller reset the device, so
+ *    its primary context and the library's module were rebuilt), it looks
+ *    the address up again, so that call too should come before any capture.
  *  - device_status: optional DEVICE pointer to a uint32 that receives the
  *    SPARK_DEVERR_* bits (OR-ed in, never cleared by the library); NULL
- *    means those faults are not reported.
+ *    means those faults are not reported.  A split that gives up on a
+ *    bounded wait (SPARK_DEVERR_TIMEOUT) leaves a neutral partial state, so
+ *    nothing an earlier call left in the buffer is merged; the output then
+ *    lacks that split's keys, and only device_status tells the caller.
  */
 #define SPARK_NOALLOC_SCRATCH_BYTES (8u << 20)
 

@@ -16,6 +16,7 @@ import pytest
 import torch
 
 import full_gqa_attention_gb300 as fga
+import oracle
 import workloads as wl
 from full_gqa_attention_gb300 import _binding as bnd
 from parity import check_close
@@ -37,20 +38,41 @@ def make_case(cuda, layer, B, H, Hkv, cap, positions, seed):
             "k": kc, "v": vc, "layer": layer}
 
 
+def oracle_want(c, k_before, v_before):
+    """The fp64 oracle's output for a case, from its caches before the call."""
+    L = c["layer"]
+    H = c["gate"].shape[1]
+    Hkv = k_before.shape[1]
+    want, _, _ = oracle.decode(wl.bf16_bits(c["qkv"].cpu()), c["gate"].cpu().numpy(),
+                               c["pos"].cpu().numpy(), wl.bf16_bits(k_before),
+                               wl.bf16_bits(v_before), L.kind, L.window, L.theta, L.rot_dim,
+                               H, Hkv, gate_mode=L.gate_mode)
+    return want
+
+
 def test_noalloc_decode_matches_workspace_decode(cuda):
     cases = [
+        # 18 splits per (sequence, KV head): the separate merge kernel
         make_case(cuda, wl.FULL_LAYER, 2, 16, 4, 20000, [19999, 7000], seed=1),
+        # 8 splits per ring at B=3: the separate merge kernel
         make_case(cuda, wl.SLIDING_LAYER, 3, 16, 4, 512, [600, 511, 40], seed=2),
+        # 64 rings: one split each, merged inside the split kernel
+        make_case(cuda, wl.SLIDING_LAYER, 64, 16, 4, 512,
+                  [513 + 37 * b for b in range(64)], seed=3),
     ]
     status = torch.zeros(1, dtype=torch.int32, device=cuda)
-    # two calls in a row, on different shapes, each against the workspace path
+    # calls in a row, on different shapes, each against the workspace path and
+    # the fp64 oracle
     for c in cases:
+        k_before, v_before = c["k"].cpu(), c["v"].cpu()
         k_ref, v_ref = c["k"].clone(), c["v"].clone()
         want = fga.spark_attn_decode(c["qkv"], c["gate"], c["pos"], k_ref, v_ref, c["layer"])
         got = fga.spark_attn_decode_noalloc(c["qkv"], c["gate"], c["pos"], c["k"], c["v"],
                                             c["layer"], device_status=status)
         torch.cuda.synchronize()
-        check_close(got, want, f"no-alloc decode kind={c['layer'].kind}")
+        what = f"no-alloc decode kind={c['layer'].kind} B={c['qkv'].shape[0]}"
+        check_close(got, want, what + " vs workspace decode")
+        check_close(got, oracle_want(c, k_before, v_before), what + " vs oracle")
         assert torch.equal(c["k"], k_ref) and torch.equal(c["v"], v_ref), "cache update differs"
     assert int(status.item()) == 0
 
