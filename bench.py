@@ -598,10 +598,12 @@ def time_small_prefill(fga, dev, bf16_peak, calls=50):
 
 def time_layer_prefill(fga, dev, bf16_peak, calls=10):
     """The whole attention block of the benchmark's prefill layer (4B
-    full_attention, B=2, T=8192, hidden 2560): q_k_v_proj and g_proj
-    (cuBLASLt), the core, out_proj (cuBLASLt), with seeded random weights of
-    the model's shapes.  Work = the three projections' flops plus the core's
-    algorithmic flops."""
+    full_attention, B=2, T=8192, hidden 2560): q_k_v_proj and g_proj (one
+    launch of the library's tcgen05 GEMM), the core, out_proj (the same GEMM),
+    with seeded random weights of the model's shapes.  Work = the three
+    projections' flops plus the core's algorithmic flops.  Beside it, the two
+    projection GEMMs alone, through spark_attn_linear and through torch.matmul
+    (cuBLAS) as a comparison that is not on the library's path."""
     import torch
     c = PREFILL
     hidden = 2560
@@ -618,37 +620,57 @@ def time_layer_prefill(fga, dev, bf16_peak, calls=10):
                                                                        c.Hkv, c.layer), dev)
     stream = torch.cuda.current_stream()
 
-    def call():
-        fga.spark_attn_layer_prefill(x, w_qkv, w_g, w_o, pos, c.layer, y=y, workspace=ws,
-                                     stream=stream)
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
 
-    for _ in range(3):
-        call()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(calls):
-        call()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / calls
+    ms = timed(lambda: fga.spark_attn_layer_prefill(x, w_qkv, w_g, w_o, pos, c.layer, y=y,
+                                                    workspace=ws, stream=stream), calls)
     rows = c.B * c.T
     proj = 2.0 * rows * hidden * (width + c.H + c.H * 256)
     flops = proj + prefill_flops(c)
+    # the projection GEMMs alone (inputs resident; x and W stay in L2 between
+    # calls, as they would inside the block)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    x2 = x.reshape(rows, hidden)
+    a = torch.randn((rows, c.H * 256), generator=g).to(torch.bfloat16).to(dev)
+    y_qkv = torch.empty((rows, width), dtype=torch.bfloat16, device=dev)
+    gemms = {}
+    for name, xx, ww, yy in (("q_k_v_proj", x2, w_qkv, y_qkv), ("out_proj", a, w_o,
+                                                                 y.reshape(rows, hidden))):
+        f = 2.0 * xx.shape[0] * xx.shape[1] * ww.shape[0]
+        t_ours = timed(lambda: fga.spark_attn_linear(xx, ww, yy, device_status=status,
+                                                     stream=stream), 20)
+        t_ref = timed(lambda: torch.matmul(xx, ww.t(), out=yy), 20)
+        gemms[name] = {"M": xx.shape[0], "N": ww.shape[0], "K": xx.shape[1], "flops": f,
+                       "ours_ms": t_ours, "ours_tflops": f / t_ours / 1e9,
+                       "ours_frac_bf16_peak": f / t_ours / 1e9 / bf16_peak,
+                       "torch_cublas_ms": t_ref, "torch_cublas_tflops": f / t_ref / 1e9}
     return {
         "workload": "attention block of the prefill layer: q_k_v_proj 2560->6144, g_proj "
                     "2560->16, core, out_proj 4096->2560 (4B, B=2 T=8192, random weights)",
         "ms": ms, "flops": flops, "projection_flops": proj,
         "tflops": flops / ms / 1e9, "frac_bf16_peak": flops / ms / 1e9 / bf16_peak,
-        "calls": calls, "projections": "cuBLASLt bf16 GEMMs, fp32 accumulation",
-        "device_status": fga.spark_attn_read_status(ws),
+        "calls": calls,
+        "projections": "library tcgen05 GEMM (q_k_v_proj and g_proj in one launch; out_proj), "
+                       "bf16 operands, fp32 accumulation in TMEM",
+        "projection_gemms": gemms,
+        "device_status": fga.spark_attn_read_status(ws) | int(status.item()),
     }
 
 
 def time_layer_decode(fga, dev, dec, hbm_peak, steps=5):
     """One decode step through all the attention blocks of the decode
     workload (the 36 layers of the 4B model at 1M context): per layer
-    q_k_v_proj and g_proj of one hidden state (cuBLASLt), the core on that
+    q_k_v_proj and g_proj of one hidden state (the library's GEMV), the core on that
     layer's cache, out_proj.  Seeded random weights of the model's shapes
     (1.9 GB for 36 layers).  Bytes = the core's KV read plus the projection
     weights, the two streams a decode step must read."""
@@ -719,7 +741,8 @@ def time_layer_decode(fga, dev, dec, hbm_peak, steps=5):
         "ms": ms, "kv_bytes": kv, "weight_bytes": weights, "gbs": gbs,
         "frac_hbm_peak": gbs / hbm_peak, "steps": steps,
         "graph_ms": graph_ms, "graph_gbs": (kv + weights) / graph_ms / 1e6,
-        "projections": "cuBLASLt bf16 GEMMs (M = 1), fp32 accumulation",
+        "projections": "library weight-streaming GEMV (M = 1; g_proj in the q_k_v_proj "
+                       "pass), fp32 accumulation",
         "device_status": status,
     }
 

@@ -84,6 +84,8 @@ def _load() -> ctypes.CDLL:
     lib.spark_attn_layer_decode.argtypes = [P, P, P, P, P, P, P, i64, D, i32, i32, i32, i32, P,
                                             P, sz, P]
     lib.spark_attn_layer_decode.restype = i32
+    lib.spark_attn_linear.argtypes = [P, P, P, i64, i32, i32, P, P]
+    lib.spark_attn_linear.restype = i32
     lib.spark_attn_read_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), i32, P]
     lib.spark_attn_read_status.restype = i32
     lib.spark_status_str.argtypes = [i32]
@@ -365,6 +367,39 @@ def spark_attn_decode_noalloc(qkv: torch.Tensor, gate: torch.Tensor, pos: torch.
     if st != SPARK_OK:
         raise SparkError(st, "spark_attn_decode_noalloc")
     return out
+
+
+def spark_attn_linear(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor | None = None,
+                      device_status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y = x W^T on the library's tcgen05 GEMM: x bf16 [..., K], w bf16 [N, K]
+    (Linear layout) -> y bf16 [..., N].  device_status: one-element 32-bit
+    CUDA tensor receiving SPARK_DEVERR_TIMEOUT (a fresh zeroed one if None;
+    with check_device_status on, that one is read and a fault raised)."""
+    _need(x, torch.bfloat16, "x")
+    _need(w, torch.bfloat16, "w")
+    N, K = w.shape
+    if x.shape[-1] != K:
+        raise ValueError("x and w disagree on K")
+    M = x.numel() // K if K else 0
+    if y is None:
+        y = torch.empty((*x.shape[:-1], N), dtype=torch.bfloat16, device=x.device)
+    _need(y, torch.bfloat16, "y")
+    if y.shape != (*x.shape[:-1], N):
+        raise ValueError("y has the wrong shape")
+    owned = device_status is None
+    if owned:
+        device_status = torch.zeros(1, dtype=torch.int32, device=x.device)
+    if not device_status.is_cuda or device_status.numel() != 1 or device_status.element_size() != 4:
+        raise ValueError("device_status must be a one-element 32-bit CUDA tensor")
+    st = lib.spark_attn_linear(_ptr(x), _ptr(w), _ptr(y), M, N, K, _ptr(device_status),
+                               _stream(stream))
+    if st != SPARK_OK:
+        raise SparkError(st, "spark_attn_linear")
+    if owned and _check_own_workspace:
+        bits = int(device_status.item())
+        if bits:
+            raise SparkDeviceFault(bits, "spark_attn_linear")
+    return y
 
 
 def _need_host(t: torch.Tensor, dtype, name: str):

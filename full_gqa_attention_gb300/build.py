@@ -27,8 +27,7 @@ def _cuda_home() -> str:
     return os.environ.get("CUDA_HOME", "/usr/local/cuda")
 
 
-# the layer calls run their projections through cuBLASLt
-LINK_FLAGS = ["-lcublasLt", "-Xlinker", "-rpath=" + os.path.join(_cuda_home(), "lib64")]
+LINK_FLAGS: list[str] = []
 
 
 def _nvcc() -> str:

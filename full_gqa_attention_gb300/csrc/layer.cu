@@ -7,24 +7,23 @@
 // (H * 256 -> hidden) maps the gated attention output back.  §1: the
 // checkpoints run in bfloat16 and the pages list no biases.
 //
-// With more than a few rows the three projections are plain dense GEMMs and
-// run through cuBLASLt (bf16 operands, fp32 accumulation) on the caller's
-// stream, with the caller's workspace as cuBLASLt's scratch; the gate GEMM
-// accumulates in fp32 and a small kernel rounds its result to bf16, the dtype
-// of the Linear's output, before the core's epilogue takes sigmoid of it in
-// fp32.  With at most kGemvMaxM rows (a decode step) they are weight-streaming
-// GEMVs of this file, g_proj in the same pass as q_k_v_proj.
-#include <cublasLt.h>
-
-#include <map>
-#include <mutex>
-#include <tuple>
-
+// With more than a few rows the projections run on the tcgen05 GEMM of
+// gemm.cu (bf16 operands, fp32 accumulation in TMEM): q_k_v_proj and g_proj
+// in one launch, whose g_proj columns leave the kernel as fp32 values rounded
+// to bf16, the dtype of the Linear's output, before the core's epilogue takes
+// the gate activation of them in fp32; then out_proj.  With at most kGemvMaxM
+// rows (a decode step) they are weight-streaming GEMVs of this file, g_proj
+// in the same pass as q_k_v_proj.
 #include "common.cuh"
 #include "spark_attn.h"
 
 namespace spark {
 
+spark_status launch_linear(const void *x, const void *w, void *y, long long M, int N, int K,
+                           const void *w2, float *y2, int N2, unsigned *status,
+                           cudaStream_t stream);
+spark_status check_linear(const void *x, const void *w, void *y, long long M, int N, int K,
+                          const void *w2, float *y2, int N2);
 spark_status prefill_impl(const void *qkv, const float *gate, const int32_t *pos,
                           const spark_layer_desc *desc, int B, int T, int H, int Hkv, void *out,
                           void *k_cache, void *v_cache, int64_t cap, const int32_t *start,
@@ -36,17 +35,6 @@ spark_status decode_impl(const void *qkv, const float *gate, const int32_t *pos,
                          void *stream, bool validate_only);
 
 namespace {
-
-constexpr size_t kLtWorkspace = 32u << 20;  // cuBLASLt scratch inside the caller's workspace
-constexpr int kMaxDevices = 64;
-
-// Rounds fp32 gate logits to bf16 precision in place (round to nearest even).
-__global__ void round_gate_kernel(float *g, long long n) {
-    grid_dep_wait();
-    grid_dep_launch();
-    const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (i < n) g[i] = __bfloat162float(__float2bfloat16_rn(g[i]));
-}
 
 // ---------------------------------------------------------------- decode GEMV
 //
@@ -134,121 +122,12 @@ cudaError_t launch_gemv(const GemvSeg &s0, const GemvSeg &s1, const void *x, int
                              static_cast<const __nv_bfloat16 *>(x), M, K);
 }
 
-std::mutex g_lt_mu;
-cublasLtHandle_t g_lt[kMaxDevices] = {};
-
-// One cuBLASLt handle per device, created on first use.
-cublasLtHandle_t lt_handle() {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lock(g_lt_mu);
-    if (!g_lt[dev] && cublasLtCreate(&g_lt[dev]) != CUBLAS_STATUS_SUCCESS) g_lt[dev] = nullptr;
-    return g_lt[dev];
-}
-
-// y[M, N] = x[M, K] * W[N, K]^T: row-major bf16 x and W (a PyTorch Linear
-// weight), y bf16 or fp32 row-major, fp32 accumulation.  In cuBLAS's
-// column-major terms: y^T (N x M) = W (stored K x N, transposed) * x^T (K x M).
-// The descriptors and the algorithm cuBLASLt's heuristic picks are kept per
-// (device, M, N, K, output type), so repeated calls skip the host-side set-up.
-struct LinearPlan {
-    cublasLtMatmulDesc_t op = nullptr;
-    cublasLtMatrixLayout_t la = nullptr, lb = nullptr, lc = nullptr;
-    cublasLtMatmulAlgo_t algo;
-    bool ok = false;
-};
-
-struct PlanKey {
-    int dev, M, N, K, y_type;
-    bool operator<(const PlanKey &o) const {
-        return std::tie(dev, M, N, K, y_type) < std::tie(o.dev, o.M, o.N, o.K, o.y_type);
-    }
-};
-
-constexpr size_t kMaxPlans = 256;
-std::mutex g_plan_mu;
-std::map<PlanKey, LinearPlan> g_plans;
-
-void destroy_plan(LinearPlan &p) {
-    if (p.lc) cublasLtMatrixLayoutDestroy(p.lc);
-    if (p.lb) cublasLtMatrixLayoutDestroy(p.lb);
-    if (p.la) cublasLtMatrixLayoutDestroy(p.la);
-    if (p.op) cublasLtMatmulDescDestroy(p.op);
-    p = LinearPlan();
-}
-
-LinearPlan make_plan(cublasLtHandle_t h, cudaDataType_t y_type, int M, int N, int K) {
-    LinearPlan p;
-    cublasLtMatmulPreference_t pref = nullptr;
-    do {
-        if (cublasLtMatmulDescCreate(&p.op, CUBLAS_COMPUTE_32F, CUDA_R_32F) !=
-            CUBLAS_STATUS_SUCCESS)
-            break;
-        const cublasOperation_t ta = CUBLAS_OP_T, tb = CUBLAS_OP_N;
-        if (cublasLtMatmulDescSetAttribute(p.op, CUBLASLT_MATMUL_DESC_TRANSA, &ta, sizeof(ta)) !=
-                CUBLAS_STATUS_SUCCESS ||
-            cublasLtMatmulDescSetAttribute(p.op, CUBLASLT_MATMUL_DESC_TRANSB, &tb, sizeof(tb)) !=
-                CUBLAS_STATUS_SUCCESS)
-            break;
-        if (cublasLtMatrixLayoutCreate(&p.la, CUDA_R_16BF, K, N, K) != CUBLAS_STATUS_SUCCESS ||
-            cublasLtMatrixLayoutCreate(&p.lb, CUDA_R_16BF, K, M, K) != CUBLAS_STATUS_SUCCESS ||
-            cublasLtMatrixLayoutCreate(&p.lc, y_type, N, M, N) != CUBLAS_STATUS_SUCCESS)
-            break;
-        if (cublasLtMatmulPreferenceCreate(&pref) != CUBLAS_STATUS_SUCCESS) break;
-        const size_t ws_bytes = kLtWorkspace;
-        if (cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES,
-                                                 &ws_bytes, sizeof(ws_bytes)) !=
-            CUBLAS_STATUS_SUCCESS)
-            break;
-        cublasLtMatmulHeuristicResult_t res;
-        int found = 0;
-        if (cublasLtMatmulAlgoGetHeuristic(h, p.op, p.la, p.lb, p.lc, p.lc, pref, 1, &res,
-                                           &found) != CUBLAS_STATUS_SUCCESS ||
-            found < 1)
-            break;
-        p.algo = res.algo;
-        p.ok = true;
-    } while (false);
-    if (pref) cublasLtMatmulPreferenceDestroy(pref);
-    if (!p.ok) destroy_plan(p);
-    return p;
-}
-
-bool linear(cublasLtHandle_t h, const void *x, const void *w, void *y, cudaDataType_t y_type,
-            int M, int N, int K, void *lt_ws, cudaStream_t stream) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return false;
-    const PlanKey key{dev, M, N, K, static_cast<int>(y_type)};
-    const float alpha = 1.0f, beta = 0.0f;
-    std::unique_lock<std::mutex> lock(g_plan_mu);
-    auto it = g_plans.find(key);
-    if (it == g_plans.end()) {
-        LinearPlan p = make_plan(h, y_type, M, N, K);
-        if (!p.ok) return false;
-        if (g_plans.size() >= kMaxPlans) {
-            // too many shapes to keep: run this one and drop its plan
-            lock.unlock();
-            const bool ok = cublasLtMatmul(h, p.op, &alpha, w, p.la, x, p.lb, &beta, y, p.lc, y,
-                                           p.lc, &p.algo, lt_ws, kLtWorkspace,
-                                           stream) == CUBLAS_STATUS_SUCCESS;
-            destroy_plan(p);
-            return ok;
-        }
-        it = g_plans.emplace(key, p).first;
-    }
-    const LinearPlan p = it->second;  // plans are never destroyed once stored
-    lock.unlock();
-    return cublasLtMatmul(h, p.op, &alpha, w, p.la, x, p.lb, &beta, y, p.lc, y, p.lc, &p.algo,
-                          lt_ws, kLtWorkspace, stream) == CUBLAS_STATUS_SUCCESS;
-}
-
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 // The layer workspace: the core's workspace first (its status word is the
-// layer's), then qkv, gate logits, the gated attention output and the
-// cuBLASLt scratch.
+// layer's), then qkv, gate logits and the gated attention output.
 struct LayerPlan {
-    size_t core, qkv, gate, attn, lt, bytes;
+    size_t core, qkv, gate, attn, bytes;
 };
 
 LayerPlan plan_layer(size_t core_bytes, long long rows, int H, int Hkv) {
@@ -257,12 +136,23 @@ LayerPlan plan_layer(size_t core_bytes, long long rows, int H, int Hkv) {
     pl.qkv = align256(core_bytes);
     pl.gate = pl.qkv + align256(static_cast<size_t>(rows) * (H + 2 * Hkv) * kHeadDim * 2);
     pl.attn = pl.gate + align256(static_cast<size_t>(rows) * H * 4);
-    pl.lt = pl.attn + align256(static_cast<size_t>(rows) * H * kHeadDim * 2);
-    pl.bytes = pl.lt + kLtWorkspace;
+    pl.bytes = pl.attn + align256(static_cast<size_t>(rows) * H * kHeadDim * 2);
     return pl;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The GEMM's own checks of both projections, before anything is enqueued
+// (rows above the GEMV's limit only: the GEMV has none to fail).
+spark_status check_layer_linears(const void *x, const void *w_qkv, const void *w_g,
+                                 const void *w_o, void *y, long long rows, int hidden, int H,
+                                 int Hkv, uint8_t *ws, const LayerPlan &pl) {
+    if (rows <= kGemvMaxM) return SPARK_OK;
+    spark_status st = check_linear(x, w_qkv, ws + pl.qkv, rows, (H + 2 * Hkv) * kHeadDim, hidden,
+                                   w_g, reinterpret_cast<float *>(ws + pl.gate), H);
+    if (st != SPARK_OK) return st;
+    return check_linear(ws + pl.attn, w_o, y, rows, hidden, H * kHeadDim, nullptr, nullptr, 0);
+}
 
 spark_status check_hidden(int hidden) {
     if (hidden <= 0) return SPARK_ERR_SHAPE;
@@ -271,9 +161,9 @@ spark_status check_hidden(int hidden) {
 }
 
 // q_k_v_proj and g_proj of `rows` hidden states into the workspace.
-spark_status project_in(cublasLtHandle_t h, const void *x, const void *w_qkv, const void *w_g,
-                        long long rows, int hidden, int H, int Hkv, uint8_t *ws,
-                        const LayerPlan &pl, cudaStream_t stream) {
+spark_status project_in(const void *x, const void *w_qkv, const void *w_g, long long rows,
+                        int hidden, int H, int Hkv, uint8_t *ws, const LayerPlan &pl,
+                        cudaStream_t stream) {
     const int M = static_cast<int>(rows);
     if (M <= kGemvMaxM) {
         // a few hidden states: one weight-streaming pass over W_qkv and W_g
@@ -283,21 +173,15 @@ spark_status project_in(cublasLtHandle_t h, const void *x, const void *w_qkv, co
         return launch_gemv(qkv, gate, x, M, hidden, stream) == cudaSuccess ? SPARK_OK
                                                                            : SPARK_ERR_CUDA;
     }
-    if (!linear(h, x, w_qkv, ws + pl.qkv, CUDA_R_16BF, M, (H + 2 * Hkv) * kHeadDim, hidden,
-                ws + pl.lt, stream) ||
-        !linear(h, x, w_g, ws + pl.gate, CUDA_R_32F, M, H, hidden, ws + pl.lt, stream))
-        return SPARK_ERR_CUDA;
-    const long long n = rows * H;
-    const cudaError_t e = launch_overlapped(round_gate_kernel,
-                                            dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256),
-                                            0, stream, reinterpret_cast<float *>(ws + pl.gate), n);
-    return e == cudaSuccess ? SPARK_OK : SPARK_ERR_CUDA;
+    // both products in one launch; the status word is the core's (workspace start)
+    return launch_linear(x, w_qkv, ws + pl.qkv, rows, (H + 2 * Hkv) * kHeadDim, hidden, w_g,
+                         reinterpret_cast<float *>(ws + pl.gate), H,
+                         reinterpret_cast<unsigned *>(ws), stream);
 }
 
 // out_proj of `rows` gated attention outputs: y = a W_o^T.
-spark_status project_out(cublasLtHandle_t h, const void *attn, const void *w_o, void *y,
-                         long long rows, int hidden, int H, uint8_t *ws, const LayerPlan &pl,
-                         cudaStream_t stream) {
+spark_status project_out(const void *attn, const void *w_o, void *y, long long rows, int hidden,
+                         int H, uint8_t *ws, cudaStream_t stream) {
     const int M = static_cast<int>(rows);
     if (M <= kGemvMaxM) {
         const GemvSeg out{static_cast<const __nv_bfloat16 *>(w_o), y, hidden, 0};
@@ -306,9 +190,8 @@ spark_status project_out(cublasLtHandle_t h, const void *attn, const void *w_o, 
                    ? SPARK_OK
                    : SPARK_ERR_CUDA;
     }
-    return linear(h, attn, w_o, y, CUDA_R_16BF, M, hidden, H * kHeadDim, ws + pl.lt, stream)
-               ? SPARK_OK
-               : SPARK_ERR_CUDA;
+    return launch_linear(attn, w_o, y, rows, hidden, H * kHeadDim, nullptr, nullptr, 0,
+                         reinterpret_cast<unsigned *>(ws), stream);
 }
 
 }  // namespace
@@ -358,15 +241,15 @@ spark_status spark_attn_layer_prefill(const void *x, const void *w_qkv, const vo
     st = prefill_impl(qkv, gate, pos, desc, B, T, H, Hkv, attn, k_cache, v_cache, cap, nullptr,
                       ws, core, stream, true);
     if (st != SPARK_OK) return st;
-    cublasLtHandle_t h = lt_handle();
-    if (!h) return SPARK_ERR_CUDA;
+    st = check_layer_linears(x, w_qkv, w_g, w_o, y, rows, hidden, H, Hkv, ws, pl);
+    if (st != SPARK_OK) return st;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    st = project_in(h, x, w_qkv, w_g, rows, hidden, H, Hkv, ws, pl, s);
+    st = project_in(x, w_qkv, w_g, rows, hidden, H, Hkv, ws, pl, s);
     if (st != SPARK_OK) return st;
     st = prefill_impl(qkv, gate, pos, desc, B, T, H, Hkv, attn, k_cache, v_cache, cap, nullptr,
                       ws, core, stream, false);
     if (st != SPARK_OK) return st;
-    return project_out(h, attn, w_o, y, rows, hidden, H, ws, pl, s);
+    return project_out(attn, w_o, y, rows, hidden, H, ws, s);
 }
 
 size_t spark_attn_layer_decode_workspace_size(int B, int hidden, int H, int Hkv, int64_t cap,
@@ -406,15 +289,15 @@ spark_status spark_attn_layer_decode(const void *x, const void *w_qkv, const voi
     st = decode_impl(qkv, gate, pos, k_cache, v_cache, cap, desc, B, H, Hkv, attn, ws, core,
                      stream, true);
     if (st != SPARK_OK) return st;
-    cublasLtHandle_t h = lt_handle();
-    if (!h) return SPARK_ERR_CUDA;
+    st = check_layer_linears(x, w_qkv, w_g, w_o, y, B, hidden, H, Hkv, ws, pl);
+    if (st != SPARK_OK) return st;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    st = project_in(h, x, w_qkv, w_g, B, hidden, H, Hkv, ws, pl, s);
+    st = project_in(x, w_qkv, w_g, B, hidden, H, Hkv, ws, pl, s);
     if (st != SPARK_OK) return st;
     st = decode_impl(qkv, gate, pos, k_cache, v_cache, cap, desc, B, H, Hkv, attn, ws, core,
                      stream, false);
     if (st != SPARK_OK) return st;
-    return project_out(h, attn, w_o, y, B, hidden, H, ws, pl, s);
+    return project_out(attn, w_o, y, B, hidden, H, ws, s);
 }
 
 }  // extern "C"

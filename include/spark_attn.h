@@ -42,8 +42,7 @@
  *    the host buffers of spark_attn_prefill_host), 16-byte aligned, dense
  *    row-major in the stated layout.  The caller owns every
  *    buffer; the library allocates no device memory and keeps no per-call
- *    state between calls (the layer calls keep one cuBLASLt handle per
- *    device).
+ *    state between calls.
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *    stream) and runs asynchronously; nothing synchronizes.
  *  - Argument errors are found on the host before anything is enqueued; the
@@ -301,10 +300,11 @@ spark_status spark_attn_decode_noalloc(const void *qkv, const float *gate, const
  * Weights use the PyTorch Linear layout (out_features x in_features, row
  * major); there are no biases.  Every product accumulates in fp32 and rounds
  * once to bf16 (the checkpoints' dtype, §1); the residual add and the norms
- * stay outside.  The projections are dense GEMMs and run through cuBLASLt on
- * `stream` (one cuBLASLt handle per device, created on the first call), with
- * the caller's workspace as its scratch.  hidden must be a positive multiple
- * of 8 (16-byte rows; else SPARK_ERR_UNSUPPORTED).
+ * stay outside.  With more than 8 rows the projections run on the library's
+ * tcgen05 GEMM (spark_attn_linear), q_k_v_proj and g_proj in one launch; with
+ * at most 8 (a decode step) on a weight-streaming GEMV, g_proj in the same
+ * pass as q_k_v_proj.  hidden must be a positive multiple of 8 (16-byte rows;
+ * else SPARK_ERR_UNSUPPORTED).
  *
  * Prefill:
  *   x  bf16 [B, T, hidden];  pos int32 [B, T];  y bf16 [B, T, hidden]
@@ -336,6 +336,24 @@ spark_status spark_attn_layer_decode(const void *x, const void *w_qkv, const voi
                                      void *v_cache, int64_t cap, const spark_layer_desc *desc,
                                      int B, int hidden, int H, int Hkv, void *y, void *workspace,
                                      size_t workspace_bytes, void *stream);
+
+/*
+ * Dense bf16 projection y = x W^T (the Linear layers around the core:
+ * Spark-X2.5 architecture, §3 Fig. 1 and §6 -- q_k_v_proj 2560 -> 6144,
+ * g_proj 2560 -> 16, out_proj 4096 -> 2560 for the 4B shapes).
+ *
+ *   x  bf16 [M, K] row major;  W  bf16 [N, K] (PyTorch Linear layout);
+ *   y  bf16 [M, N] = round-to-nearest-even of the fp32-accumulated product.
+ *
+ * Runs on the 5th-generation tensor cores (tcgen05, TMA, accumulators in
+ * TMEM), one persistent CTA per SM.  N and K must be multiples of 8 (else
+ * SPARK_ERR_UNSUPPORTED); M >= 0 (M == 0 enqueues nothing).  device_status:
+ * required DEVICE pointer to a uint32 that receives SPARK_DEVERR_TIMEOUT if a
+ * bounded wait ran out (OR-ed in, never cleared by the library).  No scratch
+ * memory is used.
+ */
+spark_status spark_attn_linear(const void *x, const void *w, void *y, int64_t M, int N, int K,
+                               uint32_t *device_status, void *stream);
 
 /*
  * Copies the sticky device status word out of a workspace (synchronizes on
