@@ -530,6 +530,9 @@ def run_ours(args, rank, world, local):
     if pre is not None and rank == 0:
         line["small_prefill"] = time_small_prefill(fga, dev, bf16_peak)
         line["layer_prefill"] = time_layer_prefill(fga, dev, bf16_peak)
+        line["layer_prefill_sliding"] = time_layer_prefill(fga, dev, bf16_peak,
+                                                           case=PREFILL_SLIDING_B2_T8192,
+                                                           compare_gemms=False)
     if dec and rank == 0:
         line["layer_decode"] = time_layer_decode(fga, dev, dec, hbm_peak)
     if pre is not None and dec and rank == 0 and not args.no_other_configs:
@@ -596,7 +599,7 @@ def time_small_prefill(fga, dev, bf16_peak, calls=50):
     }
 
 
-def time_layer_prefill(fga, dev, bf16_peak, calls=10):
+def time_layer_prefill(fga, dev, bf16_peak, calls=10, case=None, compare_gemms=True):
     """The whole attention block of the benchmark's prefill layer (4B
     full_attention, B=2, T=8192, hidden 2560): q_k_v_proj and g_proj (one
     launch of the library's tcgen05 GEMM), the core, out_proj (the same GEMM),
@@ -605,7 +608,7 @@ def time_layer_prefill(fga, dev, bf16_peak, calls=10):
     projection GEMMs alone, through spark_attn_linear and through torch.matmul
     (cuBLAS) as a comparison that is not on the library's path."""
     import torch
-    c = PREFILL
+    c = PREFILL if case is None else case
     hidden = 2560
     g = torch.Generator().manual_seed(11)
     x = torch.randn((c.B, c.T, hidden), generator=g).to(torch.bfloat16).to(dev)
@@ -637,6 +640,20 @@ def time_layer_prefill(fga, dev, bf16_peak, calls=10):
     rows = c.B * c.T
     proj = 2.0 * rows * hidden * (width + c.H + c.H * 256)
     flops = proj + prefill_flops(c)
+    kind = "full" if c.layer.kind == wl.FULL else "sliding"
+    res = {
+        "workload": f"attention block of a 4B {kind}_attention prefill layer: q_k_v_proj "
+                    f"2560->6144 (RoPE in its epilogue), g_proj 2560->16, core, out_proj "
+                    f"4096->2560 (B={c.B} T={c.T}, random weights)",
+        "ms": ms, "flops": flops, "projection_flops": proj,
+        "tflops": flops / ms / 1e9, "frac_bf16_peak": flops / ms / 1e9 / bf16_peak,
+        "calls": calls,
+        "projections": "library tcgen05 GEMM (q_k_v_proj and g_proj in one launch; out_proj), "
+                       "bf16 operands, fp32 accumulation in TMEM",
+        "device_status": fga.spark_attn_read_status(ws),
+    }
+    if not compare_gemms:
+        return res
     # the projection GEMMs alone (inputs resident; x and W stay in L2 between
     # calls, as they would inside the block)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -654,17 +671,9 @@ def time_layer_prefill(fga, dev, bf16_peak, calls=10):
                        "ours_ms": t_ours, "ours_tflops": f / t_ours / 1e9,
                        "ours_frac_bf16_peak": f / t_ours / 1e9 / bf16_peak,
                        "torch_cublas_ms": t_ref, "torch_cublas_tflops": f / t_ref / 1e9}
-    return {
-        "workload": "attention block of the prefill layer: q_k_v_proj 2560->6144, g_proj "
-                    "2560->16, core, out_proj 4096->2560 (4B, B=2 T=8192, random weights)",
-        "ms": ms, "flops": flops, "projection_flops": proj,
-        "tflops": flops / ms / 1e9, "frac_bf16_peak": flops / ms / 1e9 / bf16_peak,
-        "calls": calls,
-        "projections": "library tcgen05 GEMM (q_k_v_proj and g_proj in one launch; out_proj), "
-                       "bf16 operands, fp32 accumulation in TMEM",
-        "projection_gemms": gemms,
-        "device_status": fga.spark_attn_read_status(ws) | int(status.item()),
-    }
+    res["projection_gemms"] = gemms
+    res["device_status"] |= int(status.item())
+    return res
 
 
 def time_layer_decode(fga, dev, dec, hbm_peak, steps=5):

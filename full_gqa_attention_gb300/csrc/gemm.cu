@@ -17,6 +17,14 @@
 // the bf16-rounded result, so the gate logits leave the kernel already in the
 // Linear's output dtype.
 //
+// With rope_heads > 0 (q_k_v_proj of the attention block) the epilogue also
+// applies RoPE (§4 layered RoPE; rotate_half pairs (k, k + r/2) of the first r
+// dims, angle pos * theta^(-2k/r)) to the first rope_heads output heads, the
+// H query heads and Hkv key heads: a 256-column tile is exactly one head.  It
+// rounds the fp32 product to bf16 first (the Linear's output), then rotates in
+// fp32 and rounds again, the order and arithmetic of the attention core's own
+// rotation, so the core can run on the result without rotating.
+//
 // Warp roles:
 //   warp 0       TMA producer: per k-step of 64, the x tile (128 x 64) and the
 //                W tile (256 x 64, or N2 rounded up x 64), 128-byte swizzle,
@@ -65,11 +73,31 @@ struct GemmParams {
     void *out;          // [M, N] bf16 (row stride ldo elements)
     float *out2;        // [M, N2] fp32 holding bf16-rounded values (when N2 > 0)
     unsigned *status;   // device status word (kErrTimeout)
+    const int32_t *pos; // [M] positions of the rows (rope_heads > 0)
     int M, N, K;
     int ldo;
     int N2;             // rows of W2 (0: none)
     int m_tiles, n_tiles;  // tiles of the main product
+    int rope_heads;     // leading 256-column tiles rotated in the epilogue (0: none);
+                        // rope.rot_dim / 2 is then a multiple of 32
+    RopeTable rope;
 };
+
+// Rounds an fp32 product to bf16 and back (the Linear's bf16 output).
+__device__ __forceinline__ float round_bf16(float x) {
+    return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// Stores 32 consecutive bf16 outputs from packed pairs (masked to N).
+__device__ __forceinline__ void store32(__nv_bfloat16 *dst, const uint32_t (&pk)[16], int n0,
+                                        int N) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        if (n0 + 8 * q + 8 > N) break;
+        *reinterpret_cast<uint4 *>(dst + 8 * q) =
+            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    }
+}
 
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tm_x,
@@ -226,7 +254,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tc_fence_after();
             const int row = mt * kGemmBM + wq * 32 + lane;
             const uint32_t acc = lane_base + static_cast<uint32_t>(buf * kGemmBN);
-            if (!second) {
+            if (!second && nt >= P.rope_heads) {
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
                     const int col = wg * 128 + c * 32;
@@ -235,20 +263,62 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tmem_ld_wait();
                     const int n0 = nt * kGemmBN + col;
                     if (row < P.M) {
-                        __nv_bfloat16 *dst = out + static_cast<size_t>(row) * P.ldo + n0;
+                        uint32_t pk[16];
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            if (n0 + 8 * q + 8 > P.N) break;
-                            uint4 w;
-                            w.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]),
-                                              __uint_as_float(v[8 * q + 1]));
-                            w.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]),
-                                              __uint_as_float(v[8 * q + 3]));
-                            w.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]),
-                                              __uint_as_float(v[8 * q + 5]));
-                            w.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]),
-                                              __uint_as_float(v[8 * q + 7]));
-                            *reinterpret_cast<uint4 *>(dst + 8 * q) = w;
+                        for (int i = 0; i < 16; ++i)
+                            pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]),
+                                                __uint_as_float(v[2 * i + 1]));
+                        store32(out + static_cast<size_t>(row) * P.ldo + n0, pk, n0, P.N);
+                    }
+                }
+            } else if (!second) {
+                // a query or key head: pairs (k, k + r/2) for k < r/2, in units
+                // of 32 pairs (two 32-column chunks), then the unrotated
+                // chunks; the two warpgroups take alternate units
+                const int r = P.rope.rot_dim, half = r / 2;
+                const int npair = half / 32, nunits = npair + (kGemmBN - r) / 32;
+                const int p = row < P.M ? P.pos[row] : 0;
+                __nv_bfloat16 *dst = out + static_cast<size_t>(row < P.M ? row : 0) * P.ldo +
+                                     nt * kGemmBN;
+#pragma unroll 1
+                for (int u = wg; u < nunits; u += 2) {
+                    if (u < npair) {
+                        const int c1 = u * 32, c2 = c1 + half;
+                        uint32_t v1[32], v2[32];
+                        tmem_ld32(acc + c1, v1);
+                        tmem_ld32(acc + c2, v2);
+                        tmem_ld_wait();
+                        uint32_t pa[16], pb[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            float y[2][2];
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                float cs, sn;
+                                rope_cos_sin(p, P.rope.u[c1 + 2 * i + e], cs, sn);
+                                rope_rotate(round_bf16(__uint_as_float(v1[2 * i + e])),
+                                            round_bf16(__uint_as_float(v2[2 * i + e])), cs, sn,
+                                            y[0][e], y[1][e]);
+                            }
+                            pa[i] = pack_bf16x2(y[0][0], y[0][1]);
+                            pb[i] = pack_bf16x2(y[1][0], y[1][1]);
+                        }
+                        if (row < P.M) {
+                            store32(dst + c1, pa, nt * kGemmBN + c1, P.N);
+                            store32(dst + c2, pb, nt * kGemmBN + c2, P.N);
+                        }
+                    } else {
+                        const int c = r + (u - npair) * 32;
+                        uint32_t v[32];
+                        tmem_ld32(acc + c, v);
+                        tmem_ld_wait();
+                        if (row < P.M) {
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]),
+                                                    __uint_as_float(v[2 * i + 1]));
+                            store32(dst + c, pk, nt * kGemmBN + c, P.N);
                         }
                     }
                 }
@@ -262,9 +332,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         float *dst = P.out2 + static_cast<size_t>(row) * P.N2;
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            if (col + j < P.N2)
-                                dst[col + j] =
-                                    __bfloat162float(__float2bfloat16_rn(__uint_as_float(v[j])));
+                            if (col + j < P.N2) dst[col + j] = round_bf16(__uint_as_float(v[j]));
                     }
                 }
             }
@@ -342,12 +410,18 @@ spark_status check_linear(const void *x, const void *w, void *y, long long M, in
 }
 
 // y[M, N] = bf16(x[M, K] W[N, K]^T), and with N2 > 0 also
-// y2[M, N2] = float(bf16(x W2[N2, K]^T)).  status: device status word.
+// y2[M, N2] = float(bf16(x W2[N2, K]^T)).  status: device status word.  With
+// rope != nullptr the first rope_heads 256-column heads of y are rotated at
+// the positions pos[M] (rope->rot_dim / 2 a multiple of 32, N >= rope_heads * 256).
 spark_status launch_linear(const void *x, const void *w, void *y, long long M, int N, int K,
                            const void *w2, float *y2, int N2, unsigned *status,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, const RopeTable *rope, const int32_t *pos,
+                           int rope_heads) {
     spark_status st = check_linear(x, w, y, M, N, K, w2, y2, N2);
     if (st != SPARK_OK || M == 0) return st;
+    if (rope && rope_heads > 0 &&
+        (!pos || (rope->rot_dim / 2) % 32 != 0 || static_cast<long long>(rope_heads) * kGemmBN > N))
+        return SPARK_ERR_UNSUPPORTED;
     CUtensorMap tm_x, tm_w, tm_w2;
     std::memset(&tm_w2, 0, sizeof(tm_w2));
     if (!encode_rows(&tm_x, x, M, K, kGemmBM) || !encode_rows(&tm_w, w, N, K, kGemmBN))
@@ -365,6 +439,11 @@ spark_status launch_linear(const void *x, const void *w, void *y, long long M, i
     P.N2 = N2;
     P.m_tiles = static_cast<int>((M + kGemmBM - 1) / kGemmBM);
     P.n_tiles = (N + kGemmBN - 1) / kGemmBN;
+    if (rope && rope_heads > 0 && rope->rot_dim > 0) {
+        P.rope = *rope;
+        P.pos = pos;
+        P.rope_heads = rope_heads;
+    }
     const long long total = static_cast<long long>(P.m_tiles) * (P.n_tiles + (N2 > 0 ? 1 : 0));
     const int grid = static_cast<int>(total < gemm_sm_count() ? total : gemm_sm_count());
     cudaError_t err = cudaFuncSetAttribute(gemm_bf16_kernel,
@@ -391,5 +470,5 @@ extern "C" spark_status spark_attn_linear(const void *x, const void *w, void *y,
     if (reinterpret_cast<uintptr_t>(device_status) % 4 != 0) return SPARK_ERR_ALIGN;
     return launch_linear(x, w, y, M, N, K, nullptr, nullptr, 0,
                          reinterpret_cast<unsigned *>(device_status),
-                         static_cast<cudaStream_t>(stream));
+                         static_cast<cudaStream_t>(stream), nullptr, nullptr, 0);
 }

@@ -11,7 +11,10 @@
 // gemm.cu (bf16 operands, fp32 accumulation in TMEM): q_k_v_proj and g_proj
 // in one launch, whose g_proj columns leave the kernel as fp32 values rounded
 // to bf16, the dtype of the Linear's output, before the core's epilogue takes
-// the gate activation of them in fp32; then out_proj.  With at most kGemvMaxM
+// the gate activation of them in fp32; then out_proj.  In a prefill the same
+// epilogue also rotates Q and K (RoPE of §4, from the bf16-rounded products,
+// as the core would), so the core runs without its rotation kernel and
+// without rotating Q in the attention kernel.  With at most kGemvMaxM
 // rows (a decode step) they are weight-streaming GEMVs of this file, g_proj
 // in the same pass as q_k_v_proj.
 #include "common.cuh"
@@ -21,7 +24,9 @@ namespace spark {
 
 spark_status launch_linear(const void *x, const void *w, void *y, long long M, int N, int K,
                            const void *w2, float *y2, int N2, unsigned *status,
-                           cudaStream_t stream);
+                           cudaStream_t stream, const RopeTable *rope, const int32_t *pos,
+                           int rope_heads);
+void fill_rope_table(const spark_layer_desc *d, RopeTable *t);
 spark_status check_linear(const void *x, const void *w, void *y, long long M, int N, int K,
                           const void *w2, float *y2, int N2);
 spark_status prefill_impl(const void *qkv, const float *gate, const int32_t *pos,
@@ -160,10 +165,19 @@ spark_status check_hidden(int hidden) {
     return SPARK_OK;
 }
 
-// q_k_v_proj and g_proj of `rows` hidden states into the workspace.
+// Whether a prefill block rotates Q and K in the q_k_v_proj epilogue (the GEMM
+// path, and rotated widths it handles: r/2 a multiple of 32, so 64 and 256,
+// the two Spark-X2.5 layer types); the core then runs without rotating.
+bool rope_in_projection(long long rows, const spark_layer_desc *d) {
+    return rows > kGemvMaxM && d->rot_dim > 0 && (d->rot_dim / 2) % 32 == 0;
+}
+
+// q_k_v_proj and g_proj of `rows` hidden states into the workspace; with
+// `rope`, Q and K leave the GEMM rotated at the positions `pos`.
 spark_status project_in(const void *x, const void *w_qkv, const void *w_g, long long rows,
                         int hidden, int H, int Hkv, uint8_t *ws, const LayerPlan &pl,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, const RopeTable *rope = nullptr,
+                        const int32_t *pos = nullptr) {
     const int M = static_cast<int>(rows);
     if (M <= kGemvMaxM) {
         // a few hidden states: one weight-streaming pass over W_qkv and W_g
@@ -176,7 +190,8 @@ spark_status project_in(const void *x, const void *w_qkv, const void *w_g, long 
     // both products in one launch; the status word is the core's (workspace start)
     return launch_linear(x, w_qkv, ws + pl.qkv, rows, (H + 2 * Hkv) * kHeadDim, hidden, w_g,
                          reinterpret_cast<float *>(ws + pl.gate), H,
-                         reinterpret_cast<unsigned *>(ws), stream);
+                         reinterpret_cast<unsigned *>(ws), stream, rope, pos,
+                         rope ? H + Hkv : 0);
 }
 
 // out_proj of `rows` gated attention outputs: y = a W_o^T.
@@ -191,7 +206,7 @@ spark_status project_out(const void *attn, const void *w_o, void *y, long long r
                    : SPARK_ERR_CUDA;
     }
     return launch_linear(attn, w_o, y, rows, hidden, H * kHeadDim, nullptr, nullptr, 0,
-                         reinterpret_cast<unsigned *>(ws), stream);
+                         reinterpret_cast<unsigned *>(ws), stream, nullptr, nullptr, 0);
 }
 
 }  // namespace
@@ -244,10 +259,22 @@ spark_status spark_attn_layer_prefill(const void *x, const void *w_qkv, const vo
     st = check_layer_linears(x, w_qkv, w_g, w_o, y, rows, hidden, H, Hkv, ws, pl);
     if (st != SPARK_OK) return st;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    st = project_in(x, w_qkv, w_g, rows, hidden, H, Hkv, ws, pl, s);
-    if (st != SPARK_OK) return st;
-    st = prefill_impl(qkv, gate, pos, desc, B, T, H, Hkv, attn, k_cache, v_cache, cap, nullptr,
-                      ws, core, stream, false);
+    if (rope_in_projection(rows, desc)) {
+        // RoPE in the q_k_v_proj epilogue; the core then rotates nothing
+        RopeTable rt;
+        fill_rope_table(desc, &rt);
+        spark_layer_desc core_desc = *desc;
+        core_desc.rot_dim = 0;
+        st = project_in(x, w_qkv, w_g, rows, hidden, H, Hkv, ws, pl, s, &rt, pos);
+        if (st != SPARK_OK) return st;
+        st = prefill_impl(qkv, gate, pos, &core_desc, B, T, H, Hkv, attn, k_cache, v_cache, cap,
+                          nullptr, ws, core, stream, false);
+    } else {
+        st = project_in(x, w_qkv, w_g, rows, hidden, H, Hkv, ws, pl, s);
+        if (st != SPARK_OK) return st;
+        st = prefill_impl(qkv, gate, pos, desc, B, T, H, Hkv, attn, k_cache, v_cache, cap,
+                          nullptr, ws, core, stream, false);
+    }
     if (st != SPARK_OK) return st;
     return project_out(attn, w_o, y, rows, hidden, H, ws, s);
 }

@@ -14,6 +14,20 @@
 
 namespace spark {
 
+// u_k = theta^(-2k/r) / (2 pi) as an unevaluated fp32 pair (hi, lo).
+void fill_rope_table(const spark_layer_desc *d, RopeTable *t) {
+    std::memset(t, 0, sizeof(*t));
+    t->rot_dim = d->rot_dim;
+    const double two_pi = 6.283185307179586476925286766559;
+    for (int k = 0; k < d->rot_dim / 2; ++k) {
+        const double inv_freq = std::pow(d->rope_theta, -2.0 * k / d->rot_dim);
+        const double u = inv_freq / two_pi;
+        const float hi = static_cast<float>(u);
+        const float lo = static_cast<float>(u - static_cast<double>(hi));
+        t->u[k] = make_float2(hi, lo);
+    }
+}
+
 cudaError_t launch_decode(const CUtensorMap &tm_k, const CUtensorMap &tm_v, const DecodeParams &P,
                           cudaStream_t stream);
 cudaError_t launch_prefill(const CUtensorMap &tm_q, const CUtensorMap &tm_kv_k,
@@ -133,20 +147,6 @@ spark_status check_layer(const spark_layer_desc *d, int H, int Hkv) {
     const int G = H / Hkv;
     if (G != 1 && G != 2 && G != 4 && G != 8) return SPARK_ERR_UNSUPPORTED;
     return SPARK_OK;
-}
-
-// u_k = theta^(-2k/r) / (2 pi) as an unevaluated fp32 pair (hi, lo).
-void make_rope_table(const spark_layer_desc *d, RopeTable *t) {
-    std::memset(t, 0, sizeof(*t));
-    t->rot_dim = d->rot_dim;
-    const double two_pi = 6.283185307179586476925286766559;
-    for (int k = 0; k < d->rot_dim / 2; ++k) {
-        const double inv_freq = std::pow(d->rope_theta, -2.0 * k / d->rot_dim);
-        const double u = inv_freq / two_pi;
-        const float hi = static_cast<float>(u);
-        const float lo = static_cast<float>(u - static_cast<double>(hi));
-        t->u[k] = make_float2(hi, lo);
-    }
 }
 
 spark_status from_cuda(cudaError_t e) {
@@ -286,7 +286,7 @@ spark_status prefill_impl(const void *qkv, const float *gate, const int32_t *pos
     P.rot_w = pl.rot_w;
     P.n_qtiles = (T + tq - 1) / tq;
     P.wave = sm_count_or_default();
-    make_rope_table(desc, &P.rope);
+    fill_rope_table(desc, &P.rope);
 
     const uint64_t heads = static_cast<uint64_t>(H + 2 * Hkv);
     CUtensorMap tm_q, tm_kv_k, tm_kv_v, tm_krot, tm_out;
@@ -388,7 +388,7 @@ spark_status decode_impl(const void *qkv, const float *gate, const int32_t *pos,
     P.chunk = pl.chunk;
     P.counters = reinterpret_cast<unsigned *>(ws) + 1;  // header words after the status word
     P.fuse_merge = decode_fuses_merge(pl.nsplit, static_cast<long long>(B) * Hkv, true) ? 1 : 0;
-    make_rope_table(desc, &P.rope);
+    fill_rope_table(desc, &P.rope);
 
     // caches as [B][Hkv][cap][256]; boxes of 64 slots x 64 dims (128-byte rows)
     CUtensorMap tm_k, tm_v;
@@ -643,7 +643,7 @@ extern "C" spark_status spark_attn_decode_noalloc(const void *qkv, const float *
     // split kernel merges only where it is the only split
     P.counters = nullptr;
     P.fuse_merge = decode_fuses_merge(pl.nsplit, static_cast<long long>(B) * Hkv, false) ? 1 : 0;
-    make_rope_table(desc, &P.rope);
+    fill_rope_table(desc, &P.rope);
 
     CUtensorMap tm_k, tm_v;
     const uint64_t dims[4] = {static_cast<uint64_t>(kHeadDim), static_cast<uint64_t>(cap),

@@ -165,7 +165,7 @@ def test_layer_decode_4b(cuda, layer, cap, positions):
 @pytest.mark.parametrize("B", [1, 8, 12], ids=["gemv-1", "gemv-8", "gemm-12"])
 def test_layer_decode_batch_sizes(cuda, B):
     # up to 8 sequences the projections are the library's weight-streaming
-    # GEMV (g_proj fused with q_k_v_proj); beyond, cuBLASLt GEMMs
+    # GEMV (g_proj fused with q_k_v_proj); beyond, its tcgen05 GEMM
     layer, cap, hidden, H, Hkv = wl.SLIDING_LAYER, 512, 2560, 16, 4
     x = hidden_states((B, hidden), 45)
     w = weights(hidden, H, Hkv, 46)
@@ -178,6 +178,42 @@ def test_layer_decode_batch_sizes(cuda, B):
                                      bits(vc), layer.kind, layer.window, layer.theta,
                                      layer.rot_dim, H, Hkv)
     check_close(y, want, f"layer decode B={B}")
+
+
+@pytest.mark.parametrize("rot_dim", [64, 128, 192, 256, 16])
+@pytest.mark.parametrize("with_cache", [False, True], ids=["nocache", "cache"])
+def test_layer_prefill_rope_in_projection_is_exact(cuda, rot_dim, with_cache):
+    """The block rotates Q and K in the q_k_v_proj epilogue and runs the core
+    without rotating (rotated widths with r/2 a multiple of 32).  That must
+    give the same bits as the plain composition: the GEMM alone, the core
+    rotating itself, out_proj.  (Gate weights are zero so that both paths
+    take sigmoid(0) exactly; the fused gate column is checked against the
+    oracle above.)  r = 16 keeps the unfused path and must match too."""
+    B, T, hidden, H, Hkv = 2, 300, 512, 8, 2
+    kind = SLIDING if rot_dim in (256, 128) else FULL
+    layer = wl.Layer(kind=kind, window=100, theta=1e4 if kind == SLIDING else 5e6,
+                     rot_dim=rot_dim)
+    x = hidden_states((B, T, hidden), 60 + rot_dim).to(cuda)
+    w_qkv, _, w_o = [t.to(cuda) for t in weights(hidden, H, Hkv, 61 + rot_dim)]
+    w_g = torch.zeros((H, hidden), dtype=torch.bfloat16, device=cuda)
+    pos = (torch.arange(T, dtype=torch.int32) * 37 + 5).repeat(B, 1).to(cuda)
+    cap = T + 7
+    caches = lambda: (torch.zeros((B, Hkv, cap, D), dtype=torch.bfloat16, device=cuda),  # noqa: E731
+                      torch.zeros((B, Hkv, cap, D), dtype=torch.bfloat16, device=cuda))
+    kc1, vc1 = caches() if with_cache else (None, None)
+    kc2, vc2 = caches() if with_cache else (None, None)
+    y = fga.spark_attn_layer_prefill(x, w_qkv, w_g, w_o, pos, layer, k_cache=kc1, v_cache=vc1)
+    qkv = fga.spark_attn_linear(x, w_qkv)
+    gate = fga.spark_attn_linear(x, w_g).float()
+    if with_cache:
+        attn = fga.spark_attn_prefill_cache(qkv, gate, pos, kc2, vc2, layer)
+    else:
+        attn = fga.spark_attn_prefill(qkv, gate, pos, layer)
+    y2 = fga.spark_attn_linear(attn, w_o)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2)
+    if with_cache:
+        assert torch.equal(kc1, kc2) and torch.equal(vc1, vc2)
 
 
 def test_layer_prefill_few_rows_uses_gemv(cuda):
