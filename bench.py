@@ -1078,6 +1078,89 @@ def run_reference(args, rank, world):
     }
 
 
+# ---------------------------------------------------------------- one workload alone
+
+SINGLE = ("gemm_qkv", "gemm_out", "ring_decode_b64", "full_decode_b64", "small_prefill",
+          "prefill_sliding_T65536", "layer_prefill_full", "layer_prefill_sliding")
+
+
+def run_single(name: str, steps: int, warmup: int):
+    """Runs one workload alone, warmup + steps calls on one stream, and returns a
+    short JSON-able record with the mean time per timed call (CUDA events).  For
+    profiler captures of one kernel (ncu -s <launches to skip> -c 1)."""
+    import torch
+    import full_gqa_attention_gb300 as fga
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    g = torch.Generator(dev).manual_seed(0)
+    fn = None
+    if name in ("gemm_qkv", "gemm_out"):
+        M, N, K = (16384, 6144, 2560) if name == "gemm_qkv" else (16384, 2560, 4096)
+        x = torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16)
+        w = (torch.randn((N, K), generator=g, device=dev) / K ** 0.5).to(torch.bfloat16)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        fn = lambda: fga.spark_attn_linear(x, w, y, device_status=st)  # noqa: E731
+        work = {"flops": 2.0 * M * N * K}
+    elif name in ("ring_decode_b64", "full_decode_b64"):
+        c = wl.DECODE_SLIDING_4B_B64 if name == "ring_decode_b64" else wl.DECODE_FULL_4B_B64
+        step = wl.make_decode_step_inputs(c)
+        k = torch.empty((c.B, c.Hkv, c.cap, 256), dtype=torch.bfloat16, device=dev)
+        v = torch.empty_like(k)
+        k.normal_(generator=g)
+        v.normal_(generator=g)
+        q, gt, p = (step[n].to(dev) for n in ("qkv", "gate", "pos"))
+        o = torch.empty((c.B, c.H * 256), dtype=torch.bfloat16, device=dev)
+        ws = fga.new_workspace(fga.spark_attn_decode_workspace_size(c.B, c.H, c.Hkv, c.cap,
+                                                                    c.layer), dev)
+        fn = lambda: fga.spark_attn_decode(q, gt, p, k, v, c.layer, out=o, workspace=ws)  # noqa: E731
+        lens = step["pos"].long() + 1
+        vis = lens if c.layer.kind == wl.FULL else lens.clamp(max=c.layer.window)
+        work = {"kv_bytes": int(vis.sum()) * KV_BYTES_PER_TOKEN}
+    elif name in ("small_prefill", "prefill_sliding_T65536"):
+        c = wl.PREFILL_SLIDING_1P7B_T1024 if name == "small_prefill" else wl.PREFILL_SLIDING_4B_T65536
+        x = wl.make_prefill_inputs(c)
+        q, gt, p = (x[n].to(dev) for n in ("qkv", "gate", "pos"))
+        o = torch.empty((c.B, c.T, c.H * 256), dtype=torch.bfloat16, device=dev)
+        ws = fga.new_workspace(fga.spark_attn_prefill_workspace_size(c.B, c.T, c.H, c.Hkv,
+                                                                     c.layer), dev)
+        fn = lambda: fga.spark_attn_prefill(q, gt, p, c.layer, out=o, workspace=ws)  # noqa: E731
+        work = {"flops": prefill_flops(c)}
+    elif name in ("layer_prefill_full", "layer_prefill_sliding"):
+        c = PREFILL if name == "layer_prefill_full" else PREFILL_SLIDING_B2_T8192
+        hidden, width = 2560, (c.H + 2 * c.Hkv) * 256
+        x = torch.randn((c.B, c.T, hidden), generator=g, device=dev).to(torch.bfloat16)
+        w_qkv = (torch.randn((width, hidden), generator=g, device=dev) / hidden ** 0.5).to(
+            torch.bfloat16)
+        w_g = (torch.randn((c.H, hidden), generator=g, device=dev) / hidden ** 0.5).to(
+            torch.bfloat16)
+        w_o = (torch.randn((hidden, c.H * 256), generator=g, device=dev) / 64.0).to(
+            torch.bfloat16)
+        pos = torch.arange(c.T, dtype=torch.int32, device=dev).repeat(c.B, 1)
+        y = torch.empty((c.B, c.T, hidden), dtype=torch.bfloat16, device=dev)
+        ws = fga.new_workspace(fga.spark_attn_layer_prefill_workspace_size(
+            c.B, c.T, hidden, c.H, c.Hkv, c.layer), dev)
+        fn = lambda: fga.spark_attn_layer_prefill(x, w_qkv, w_g, w_o, pos, c.layer, y=y,  # noqa: E731
+                                                  workspace=ws)
+        work = {"flops": 2.0 * c.B * c.T * hidden * (width + c.H + c.H * 256) + prefill_flops(c)}
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / max(steps, 1)
+    rec = {"single": name, "steps": steps, "warmup": warmup, "ms_per_call": ms, **work}
+    if "flops" in work:
+        rec["tflops"] = work["flops"] / ms / 1e9
+    if "kv_bytes" in work:
+        rec["kv_gbs"] = work["kv_bytes"] / ms / 1e6
+    return rec
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -1092,10 +1175,15 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other-configs", action="store_true",
                     help="skip the extra lines for the long prefill and the batched decode")
+    ap.add_argument("--single", choices=SINGLE, default=None,
+                    help="time one workload alone (for profiler captures of one kernel)")
     ap.add_argument("--prefill-layer", choices=("full", "sliding"), default="full",
                     help="layer type of the prefill workload (sliding: for profiling; the "
                          "benchmark's workload is the full layer)")
     args = ap.parse_args(argv)
+    if args.single:
+        print(json.dumps(run_single(args.single, args.steps, args.warmup)), flush=True)
+        return
     if args.warmup < 3 and args.impl == "ours":
         print("bench.py: warmup raised to 3", file=sys.stderr)
         args.warmup = 3

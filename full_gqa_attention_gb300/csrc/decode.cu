@@ -270,6 +270,56 @@ __device__ __forceinline__ void merge_head_in_split(const DecodeParams &P, int b
     store_head(P, b, g, hq, h, p, d0, acc, L, nt, gate_logit);
 }
 
+// The same merge where the scan has one split: that split's state is the
+// CTA's own, still in shared memory (the per-warp maxima, sums and rescaled
+// outputs of the final reduction), so it is summed there in the order the
+// global partial state would have been, with no round trip through L2.  A
+// CTA that gave up on a wait merges a neutral state.
+__device__ __forceinline__ void merge_head_local(const DecodeParams &P, int b, int g, int hq,
+                                                 long long p, int lane, const NewToken &nt,
+                                                 float gate_logit, const float *red_o,
+                                                 const float (&red_m)[kDecWarps][8],
+                                                 const float (&red_l)[kDecWarps][8],
+                                                 bool aborted) {
+    const int h = g * P.G + hq, d0 = lane * 8;
+    float2 ml[kFuseMaxSplits];
+    float4 pa[kFuseMaxSplits], pc[kFuseMaxSplits];
+#pragma unroll
+    for (int sp = 0; sp < kFuseMaxSplits; ++sp) {
+        ml[sp] = make_float2(-INFINITY, 0.f);
+        pa[sp] = pc[sp] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (!aborted) {
+        float M = red_m[0][hq];
+#pragma unroll
+        for (int w = 1; w < kDecWarps; ++w) M = fmaxf(M, red_m[w][hq]);
+        float L = 0.f;
+        if (M != -INFINITY)
+#pragma unroll
+            for (int w = 0; w < kDecWarps; ++w) L += red_l[w][hq] * fast_exp2(red_m[w][hq] - M);
+        ml[0] = make_float2(M, L);
+        float o[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float a = 0.f;
+#pragma unroll
+            for (int w = 0; w < kDecWarps; ++w) a += red_o[(w * 8 + hq) * kHeadDim + d0 + i];
+            o[i] = a;
+        }
+        pa[0] = make_float4(o[0], o[1], o[2], o[3]);
+        pc[0] = make_float4(o[4], o[5], o[6], o[7]);
+    }
+    float M = nt.x_new;
+#pragma unroll
+    for (int sp = 0; sp < kFuseMaxSplits; ++sp) M = fmaxf(M, ml[sp].x);
+    float acc[8], L;
+    if (merge_warps(P.G) == kMergeWarps)
+        merge_parts<kMergeWarps>(nt, M, 1, ml, pa, pc, acc, L);
+    else
+        merge_parts<2>(nt, M, 1, ml, pa, pc, acc, L);
+    store_head(P, b, g, hq, h, p, d0, acc, L, nt, gate_logit);
+}
+
 // kFuse: this CTA's grid merges itself (P.fuse_merge); a separate
 // instantiation, so that the kernel of the long scans carries none of it.
 template <int kDecStages, bool kFuse>
@@ -297,27 +347,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     grid_dep_wait();  // inputs and cache may come from the previous kernel
-    const long long p = P.pos[b];
-    if (p < 0 || (P.kind == kLayerFull && p >= P.cap)) {
-        if (split == 0 && g == 0 && tid == 0) atomicOr(P.status, kErrPosition);
-        return;
-    }
-    // Scanned slots: full layer -> tokens [0, pos); ring -> slots [0, min(pos, cap)).
-    const long long n_scan = decode_scan_slots(P.kind, p, P.cap);
     const long long c_lo = static_cast<long long>(split) * P.chunk;
-    const long long c_hi = (c_lo + P.chunk < n_scan) ? c_lo + P.chunk : n_scan;
-    if (c_lo >= c_hi) {
-        // An empty split: the merge does not read it.  With nothing cached yet
-        // no split has work, and a fused merge then comes from split 0, on the
-        // new token alone.
-        if (kFuse && n_scan == 0 && split == 0 && warp < kDecWarps)
-            for (int hq = warp; hq < P.G; hq += kDecWarps)
-                merge_head_in_split(P, b, g, hq, p, 0, lane,
-                                    score_new_token(P, b, g, g * P.G + hq, p, lane),
-                                    P.gate[static_cast<size_t>(b) * P.H + g * P.G + hq]);
-        return;
-    }
-    const int ntiles = static_cast<int>((c_hi - c_lo + kDecTile - 1) / kDecTile);
 
     // one tile of K and V into stage t % kDecStages
     auto issue_tile = [&](int t) {
@@ -333,10 +363,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
             tma_load_4d(kt + kDecTileBytes + c * (kDecTileBytes / 4), &tm_v, &full[s], c * 64,
                         key0, g, b);
     };
-    // The producer sets the stages up and starts the first loads at once: they
-    // do not depend on the query prologue below, which they overlap.
-    const int n_pre = ntiles < kDecStages ? ntiles : kDecStages;
-    if (tid == kDecWarps * 32) {
+    auto init_stages = [&]() {
         for (int s = 0; s < kDecStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kDecWarps);
@@ -345,6 +372,44 @@ __global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
         abort_flag = 0;
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
+    };
+    // The one-stage kernels (short scans: every CTA of a batch of rings starts
+    // at once) load their first tile before the position is read, so the
+    // position's latency overlaps the copy.  A split's first slots always lie
+    // inside the cache (chunk * split < the longest scan <= cap); a CTA that
+    // turns out to have no work waits for the copy to land before it exits.
+    constexpr bool kSpeculate = kDecStages == 1;
+    const bool producer = tid == kDecWarps * 32;
+    if (kSpeculate && producer) {
+        init_stages();
+        issue_tile(0);
+    }
+
+    const long long p = P.pos[b];
+    const bool bad_pos = p < 0 || (P.kind == kLayerFull && p >= P.cap);
+    // Scanned slots: full layer -> tokens [0, pos); ring -> slots [0, min(pos, cap)).
+    const long long n_scan = bad_pos ? 0 : decode_scan_slots(P.kind, p, P.cap);
+    const long long c_hi = (c_lo + P.chunk < n_scan) ? c_lo + P.chunk : n_scan;
+    if (bad_pos || c_lo >= c_hi) {
+        if (bad_pos && split == 0 && g == 0 && tid == 0) atomicOr(P.status, kErrPosition);
+        // An empty split: the merge does not read it.  With nothing cached yet
+        // no split has work, and a fused merge then comes from split 0, on the
+        // new token alone.
+        if (kFuse && !bad_pos && n_scan == 0 && split == 0 && warp < kDecWarps)
+            for (int hq = warp; hq < P.G; hq += kDecWarps)
+                merge_head_in_split(P, b, g, hq, p, 0, lane,
+                                    score_new_token(P, b, g, g * P.G + hq, p, lane),
+                                    P.gate[static_cast<size_t>(b) * P.H + g * P.G + hq]);
+        if (kSpeculate && producer) mbar_wait_plain(&full[0], 0);
+        return;
+    }
+    const int ntiles = static_cast<int>((c_hi - c_lo + kDecTile - 1) / kDecTile);
+
+    // The producer sets the stages up and starts the first loads at once: they
+    // do not depend on the query prologue below, which they overlap.
+    const int n_pre = ntiles < kDecStages ? ntiles : kDecStages;
+    if (!kSpeculate && producer) {
+        init_stages();
         for (int t = 0; t < n_pre; ++t) issue_tile(t);
     }
 
@@ -543,6 +608,9 @@ __global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
         red_l[warp][h1] = l1;
     }
     named_bar_sync(1, kDecWarps * 32);
+    // With one split per (sequence, KV head) a merging kernel merges from the
+    // reduction buffers in shared memory; no partial state goes to global memory.
+    const bool local_merge = kFuse && P.nsplit == 1;
     // abort_flag is stable here: it is only raised inside a wait, and every
     // wait of the producer and the consumers has returned.
     if (!abort_flag) {
@@ -566,14 +634,14 @@ __global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
         }
         named_bar_sync(1, kDecWarps * 32);
         const size_t part0 = (static_cast<size_t>(b) * P.H + static_cast<size_t>(g) * P.G) * P.nsplit;
-        for (int i = tid; i < P.G * kHeadDim; i += kDecWarps * 32) {
+        for (int i = tid; !local_merge && i < P.G * kHeadDim; i += kDecWarps * 32) {
             const int hh = i / kHeadDim, d = i % kHeadDim;
             float acc = 0.f;
 #pragma unroll
             for (int w = 0; w < kDecWarps; ++w) acc += red_o[(w * 8 + hh) * kHeadDim + d];
             P.part_o[(part0 + static_cast<size_t>(hh) * P.nsplit + split) * kHeadDim + d] = acc;
         }
-        if (tid < P.G) {
+        if (!local_merge && tid < P.G) {
             const int hh = tid;
             float M = red_m[0][hh];
             for (int w = 1; w < kDecWarps; ++w) M = fmaxf(M, red_m[w][hh]);
@@ -584,7 +652,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
             *reinterpret_cast<float2 *>(P.part_ml + 2 * (part0 + static_cast<size_t>(hh) * P.nsplit +
                                                          split)) = ml;
         }
-    } else {
+    } else if (!local_merge) {
         // A wait gave up (the status word says so): leave a neutral state
         // (max -inf, sum 0, output 0), which the merge weighs by 0, so that
         // it never merges what an earlier call left in a shared buffer.
@@ -628,6 +696,18 @@ __global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
         named_bar_sync(1, kDecWarps * 32);
         if (!last_cta) return;
         __threadfence();  // order the reads of the other splits' states after the count
+    }
+    if (local_merge) {
+        const float *red_o = reinterpret_cast<const float *>(stages);
+        const bool aborted = abort_flag != 0;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int hq = warp + i * kDecWarps;
+            if (hq < P.G)
+                merge_head_local(P, b, g, hq, p, lane, nt[i], gq[hq], red_o, red_m, red_l,
+                                 aborted);
+        }
+        return;
     }
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
