@@ -805,8 +805,10 @@ def time_other_configs(fga, dev, bf16_peak, hbm_peak):
         o = torch.empty((c.B, c.H * 256), dtype=torch.bfloat16, device=dev)
         ws = fga.new_workspace(fga.spark_attn_decode_workspace_size(c.B, c.H, c.Hkv, c.cap,
                                                                     c.layer), dev)
+        # ~30 us per ring call: 50 calls so that the events' own overhead is small
+        calls = 10 if c.layer.kind == wl.FULL else 50
         ms = timed(lambda: fga.spark_attn_decode(q, g, p, k, v, c.layer, out=o, workspace=ws,
-                                                 stream=stream), 10)
+                                                 stream=stream), calls)
         # visible tokens per sequence, the new one included (as for the step's decode)
         lens = step["pos"].long() + 1
         visible = lens if c.layer.kind == wl.FULL else lens.clamp(max=c.layer.window)

@@ -44,7 +44,7 @@ constexpr int kDecQBytes = 8 * kHeadDim * 2;              // 8 (padded) query he
 constexpr int kDecNewBytes = 2 * kHeadDim * 2 + 8 * 4;
 constexpr int dec_smem_bytes(int stages, bool fuse) {
     return 1024 + stages * kDecStageBytes + kDecQBytes + (fuse ? kDecNewBytes : 0) +
-           2 * stages * 8;
+           3 * stages * 8;
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
@@ -339,6 +339,9 @@ __global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kDecStages * kDecStageBytes + kDecQBytes +
                                                   (kFuse ? kDecNewBytes : 0));
     uint64_t *empty = full + kDecStages;
+    // K and V of a stage land on separate barriers: the scores and the softmax
+    // of a tile run while its V is still arriving
+    uint64_t *fullv = empty + kDecStages;
     __shared__ int abort_flag;
     __shared__ float red_m[kDecWarps][8];
     __shared__ float red_l[kDecWarps][8];
@@ -352,20 +355,22 @@ __global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
     // one tile of K and V into stage t % kDecStages
     auto issue_tile = [&](int t) {
         const int s = t % kDecStages;
-        mbar_arrive_expect_tx(&full[s], kDecStageBytes);
         const int key0 = static_cast<int>(c_lo + static_cast<long long>(t) * kDecTile);
         uint8_t *kt = stages + s * kDecStageBytes;
+        mbar_arrive_expect_tx(&full[s], kDecTileBytes);
 #pragma unroll
         for (int c = 0; c < 4; ++c)
             tma_load_4d(kt + c * (kDecTileBytes / 4), &tm_k, &full[s], c * 64, key0, g, b);
+        mbar_arrive_expect_tx(&fullv[s], kDecTileBytes);
 #pragma unroll
         for (int c = 0; c < 4; ++c)
-            tma_load_4d(kt + kDecTileBytes + c * (kDecTileBytes / 4), &tm_v, &full[s], c * 64,
+            tma_load_4d(kt + kDecTileBytes + c * (kDecTileBytes / 4), &tm_v, &fullv[s], c * 64,
                         key0, g, b);
     };
     auto init_stages = [&]() {
         for (int s = 0; s < kDecStages; ++s) {
             mbar_init(&full[s], 1);
+            mbar_init(&fullv[s], 1);
             mbar_init(&empty[s], kDecWarps);
         }
         fence_mbar_init();
@@ -400,7 +405,10 @@ __global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
                 merge_head_in_split(P, b, g, hq, p, 0, lane,
                                     score_new_token(P, b, g, g * P.G + hq, p, lane),
                                     P.gate[static_cast<size_t>(b) * P.H + g * P.G + hq]);
-        if (kSpeculate && producer) mbar_wait_plain(&full[0], 0);
+        if (kSpeculate && producer) {
+            mbar_wait_plain(&full[0], 0);
+            mbar_wait_plain(&fullv[0], 0);
+        }
         return;
     }
     const int ntiles = static_cast<int>((c_hi - c_lo + kDecTile - 1) / kDecTile);
@@ -477,8 +485,10 @@ __global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
         // releases its shared memory.
         if (lane == 0 && abort_flag) {
             const int first = issued > kDecStages ? issued - kDecStages : 0;
-            for (int t = first; t < issued; ++t)
+            for (int t = first; t < issued; ++t) {
                 mbar_wait_plain(&full[t % kDecStages], (t / kDecStages) & 1);
+                mbar_wait_plain(&fullv[t % kDecStages], (t / kDecStages) & 1);
+            }
         }
         return;
     }
@@ -521,26 +531,6 @@ __global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
             mma_bf16_16816(sc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
         }
 
-        // Slots past the chunk end may hold anything (even NaN bit patterns in
-        // a cache that was never written there); their probabilities are 0,
-        // but 0 * NaN is NaN in P*V, so this warp zeroes its V rows past the end.
-        {
-            const long long row0 = c_lo + static_cast<long long>(t) * kDecTile + warp * 16;
-            if (row0 + 16 > c_hi) {
-                uint8_t *vrows = stages + s * kDecStageBytes + kDecTileBytes;
-                for (int rr = 0; rr < 16; ++rr) {
-                    if (row0 + rr < c_hi) continue;
-                    const int vr = warp * 16 + rr;  // 4 chunks of 128 bytes per row
-                    *reinterpret_cast<uint4 *>(vrows + (lane >> 3) * (kDecTileBytes / 4) +
-                                               vr * 128 + (lane & 7) * 16) =
-                        make_uint4(0, 0, 0, 0);
-                }
-                // the stage is refilled by TMA later: order these writes first
-                fence_proxy_async_smem();
-                __syncwarp();
-            }
-        }
-
         // this thread's two slots (rows lane/4 and lane/4 + 8) and two heads
         const long long sa = c_lo + static_cast<long long>(t) * kDecTile + warp * 16 + (lane >> 2);
         const long long sb = sa + 8;
@@ -580,6 +570,27 @@ __global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
         // P^T as the B operand of O^T += V^T P^T (transpose of the score fragment)
         const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
         const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
+        if (!mbar_wait(&fullv[s], (t / kDecStages) & 1, &abort_flag, P.status)) break;
+
+        // Slots past the chunk end may hold anything (even NaN bit patterns in
+        // a cache that was never written there); their probabilities are 0,
+        // but 0 * NaN is NaN in P*V, so this warp zeroes its V rows past the end.
+        {
+            const long long row0 = c_lo + static_cast<long long>(t) * kDecTile + warp * 16;
+            if (row0 + 16 > c_hi) {
+                uint8_t *vrows = stages + s * kDecStageBytes + kDecTileBytes;
+                for (int rr = 0; rr < 16; ++rr) {
+                    if (row0 + rr < c_hi) continue;
+                    const int vr = warp * 16 + rr;  // 4 chunks of 128 bytes per row
+                    *reinterpret_cast<uint4 *>(vrows + (lane >> 3) * (kDecTileBytes / 4) +
+                                               vr * 128 + (lane & 7) * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
+                // the stage is refilled by TMA later: order these writes first
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+        }
 #pragma unroll
         for (int db = 0; db < 16; ++db) {
             const int gran = ((db * 16) & 63) / 8 + ((lane >> 3) & 1);
@@ -627,10 +638,15 @@ __global__ void __launch_bounds__(kDecThreads, kDecStages == 1 ? 2 : 1)
 #pragma unroll
         for (int db = 0; db < 16; ++db) {
             const int d = db * 16 + (lane >> 2);
-            red_o[(warp * 8 + h0) * kHeadDim + d] = o[db][0] * s0;
-            red_o[(warp * 8 + h1) * kHeadDim + d] = o[db][1] * s1;
-            red_o[(warp * 8 + h0) * kHeadDim + d + 8] = o[db][2] * s0;
-            red_o[(warp * 8 + h1) * kHeadDim + d + 8] = o[db][3] * s1;
+            // only the group's G heads are read back (heads G..7 are padding)
+            if (h0 < P.G) {
+                red_o[(warp * 8 + h0) * kHeadDim + d] = o[db][0] * s0;
+                red_o[(warp * 8 + h0) * kHeadDim + d + 8] = o[db][2] * s0;
+            }
+            if (h1 < P.G) {
+                red_o[(warp * 8 + h1) * kHeadDim + d] = o[db][1] * s1;
+                red_o[(warp * 8 + h1) * kHeadDim + d + 8] = o[db][3] * s1;
+            }
         }
         named_bar_sync(1, kDecWarps * 32);
         const size_t part0 = (static_cast<size_t>(b) * P.H + static_cast<size_t>(g) * P.G) * P.nsplit;
