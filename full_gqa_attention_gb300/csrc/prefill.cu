@@ -14,7 +14,8 @@
 //       Warp roles:
 //         warp 0       TMA producer (Q tile once, then K and V through a ring
 //                      of 16 KB slots)
-//         warp 1       TMEM owner and MMA issuer (one thread)
+//         warp 1       TMEM owner and QK^T issuer (one thread)
+//         warp 2       P*V issuer (one thread)
 //         warps 4..11  softmax, two warpgroups: query row i (TMEM lane i) is
 //                      shared by thread i of each; warpgroup w owns score
 //                      columns [64w, 64w+64) and output dims [128w, 128w+128)
@@ -317,6 +318,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (i == kBarQReady || i == kBarPReady || i == kBarPReady + 1 || i == kBarMaxX ||
                 i == kBarMaxX + 1)
                 count = kSoftmaxThreads;
+            if (i == kBarMmaDrain) count = 2;  // one commit from each MMA issuer
             mbar_init(&bars[i], count);
         }
         fence_mbar_init();
@@ -454,10 +456,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int s = first; s < sc; ++s)
                 mbar_wait_plain(&bars[kBarSlotFull + (s % kSlots)], (s / kSlots) & 1);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == 2) {
+        // ------------------------------------------------------ MMA issuers
+        // Two threads issue the products: warp 1's lane 0 the QK^T of every
+        // key tile, warp 2's lane 0 every P*V, so neither waits for the
+        // other's issue.  Both replay the producer's load order (K0, K1, then
+        // per tile j: V_j, K_{j+2}) to find the ring slots of their chunks.
+        // The barriers carry the dependencies between them: P*V of tile j
+        // waits for P_j (softmax), and QK^T of tile j+2, which overwrites the
+        // score buffer holding P_j, waits for P*V of tile j to complete.
+        const bool qk_role = warp == 1;
         if (lane == 0 && !skip) {
-            int sc = 0;
             // Shared-memory descriptors built once: the address field holds
             // (address mod 2^18) / 16 in its low bits, and every operand lies
             // below 2^18, so an operand at byte offset o from a base has the
@@ -469,8 +478,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             // descriptor in place)
             constexpr bool kDescInPlace = kSrc == kKvFromCache;
             const uint32_t q_addr = smem_u32(qbuf), ring_addr = smem_u32(ring);
-            bool ok = mbar_wait(&bars[kBarQReady], 0, &abort_flag, P.status);
-            tc_fence_after();
+            int sc = 0;  // ring slots of the producer's loads before the next one
+            bool ok = true;
             auto mma_qk = [&](int j) -> bool {
                 const uint32_t d = tmem + kColS + (j & 1) * kBN;
                 for (int c = 0; c < 4; ++c) {
@@ -523,30 +532,43 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 tc_commit(&bars[kBarODone]);
                 return true;
             };
-            if (ok) ok = mma_qk(0);
-            if (ok && ntiles > 1) ok = mma_qk(1);
-            for (int j = 0; ok && j < ntiles; ++j) {
-                ok = mbar_wait(&bars[kBarPReady + (j & 1)], (j >> 1) & 1, &abort_flag, P.status);
-                if (!ok) break;
+            if (qk_role) {
+                ok = mbar_wait(&bars[kBarQReady], 0, &abort_flag, P.status);
                 tc_fence_after();
-                ok = mma_pv(j);
-                if (ok && j + 2 < ntiles) {
-                    // QK^T of tile j+2 overwrites the score buffer whose first
-                    // half holds P_j.  tcgen05.mma keeps issue order only among
-                    // products into the same accumulator, so wait until P*V of
-                    // tile j (accumulator O) has finished reading P_j.
-                    ok = mbar_wait(&bars[kBarODone], j & 1, &abort_flag, P.status);
-                    if (ok) {
-                        tc_fence_after();
-                        ok = mma_qk(j + 2);
+                if (ok) ok = mma_qk(0);
+                if (ok && ntiles > 1) ok = mma_qk(1);
+                for (int j = 0; ok && j < ntiles; ++j) {
+                    sc += 4;  // V_j: the other issuer's
+                    if (j + 2 < ntiles) {
+                        // QK^T of tile j+2 overwrites the score buffer whose
+                        // first half holds P_j: wait until P*V of tile j
+                        // (accumulator O) has finished reading it.  P*V of tile
+                        // j+1 needs QK^T of tile j+1, issued before this wait,
+                        // so the barrier is never two phases ahead of it.
+                        ok = mbar_wait(&bars[kBarODone], j & 1, &abort_flag, P.status);
+                        if (ok) {
+                            tc_fence_after();
+                            ok = mma_qk(j + 2);
+                        }
                     }
                 }
+            } else {
+                sc = ntiles > 1 ? 8 : 4;  // after K0 and K1
+                for (int j = 0; ok && j < ntiles; ++j) {
+                    ok = mbar_wait(&bars[kBarPReady + (j & 1)], (j >> 1) & 1, &abort_flag,
+                                   P.status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    ok = mma_pv(j);
+                    if (j + 2 < ntiles) sc += 4;  // K_{j+2}: the other issuer's
+                }
+                // The epilogue waits on a barrier of its own: a parity wait on
+                // kBarODone could be two phases behind when the last softmax
+                // tile finishes before P*V of the tile before it.
+                if (ok) tc_commit(&bars[kBarOFinal]);
             }
-            // The epilogue waits on a barrier of its own: a parity wait on
-            // kBarODone could be two phases behind when the last softmax tile
-            // finishes before P*V of the tile before it.
-            if (ok) tc_commit(&bars[kBarOFinal]);
-            // every MMA issued so far must finish before TMEM is released
+            // every product either thread issued must finish before TMEM is
+            // released (the drain barrier counts one arrival from each)
             tc_commit(&bars[kBarMmaDrain]);
             mbar_wait_plain(&bars[kBarMmaDrain], 0);
         }
@@ -554,7 +576,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        if (qk_role) tmem_dealloc(tmem, kTmemCols);
     } else if (warp >= kSoftmaxWarp0) {
         // ------------------------------------------------------ softmax
         const int wq = warp & 3;                        // TMEM lane quarter of this warp
@@ -716,7 +738,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc_fence_before();
         __syncthreads();
     } else {
-        // warps 2 and 3 have no role yet
+        // warp 3 has no role
         __syncthreads();
     }
 }
