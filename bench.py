@@ -826,11 +826,12 @@ def time_other_configs(fga, dev, bf16_peak, hbm_peak):
 # Per-launch DRAM traffic (read + write bytes) from ncu captures of the
 # current kernels, scaled to one launch of the bench workload; None when the
 # kernels changed since the counters were taken.
-# decode_split_kernel: 540.5 MB in a 131,072-token capture, scaled x8 to the
-# 1,048,576-token layer; prefill_attn_kernel: 492.2 MB measured on this workload.
+# prefill_attn_kernel: 393.4 MB read + 100.3 MB written, measured on this
+# workload (the two-issuer kernel).  decode_split_kernel: not yet re-measured
+# since its K and V barriers were split, so None.
 TRAFFIC: dict[str, float | None] = {
-    "decode_split_kernel": 540.474624e6 * 8,
-    "prefill_attn_kernel": 492.185344e6,
+    "decode_split_kernel": None,
+    "prefill_attn_kernel": 493.713152e6,
 }
 
 
@@ -1083,7 +1084,8 @@ def run_reference(args, rank, world):
 # ---------------------------------------------------------------- one workload alone
 
 SINGLE = ("gemm_qkv", "gemm_out", "ring_decode_b64", "full_decode_b64", "small_prefill",
-          "prefill_sliding_T65536", "layer_prefill_full", "layer_prefill_sliding")
+          "prefill_full_B2_T8192", "prefill_sliding_B2_T8192", "prefill_sliding_T65536",
+          "layer_prefill_full", "layer_prefill_sliding")
 
 
 def run_single(name: str, steps: int, warmup: int):
@@ -1119,8 +1121,11 @@ def run_single(name: str, steps: int, warmup: int):
         lens = step["pos"].long() + 1
         vis = lens if c.layer.kind == wl.FULL else lens.clamp(max=c.layer.window)
         work = {"kv_bytes": int(vis.sum()) * KV_BYTES_PER_TOKEN}
-    elif name in ("small_prefill", "prefill_sliding_T65536"):
-        c = wl.PREFILL_SLIDING_1P7B_T1024 if name == "small_prefill" else wl.PREFILL_SLIDING_4B_T65536
+    elif name in ("small_prefill", "prefill_full_B2_T8192", "prefill_sliding_B2_T8192",
+                  "prefill_sliding_T65536"):
+        c = {"small_prefill": wl.PREFILL_SLIDING_1P7B_T1024, "prefill_full_B2_T8192": PREFILL,
+             "prefill_sliding_B2_T8192": PREFILL_SLIDING_B2_T8192,
+             "prefill_sliding_T65536": wl.PREFILL_SLIDING_4B_T65536}[name]
         x = wl.make_prefill_inputs(c)
         q, gt, p = (x[n].to(dev) for n in ("qkv", "gate", "pos"))
         o = torch.empty((c.B, c.T, c.H * 256), dtype=torch.bfloat16, device=dev)
