@@ -707,23 +707,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tc_fence_after();
             const float l_row = l_part + red_l[wg ^ 1][row];
             const float scale = valid ? gate_act(gate_logit, P.gate_mode) / l_row : 0.f;
-            for (int c = wg * 128; c < wg * 128 + 128; c += 32) {
-                uint32_t ov[32];
-                tmem_ld32(lane_base + kColO + c, ov);
+            // two 32-column loads in flight per wait (the loads' latency overlaps)
+            for (int c = wg * 128; c < wg * 128 + 128; c += 64) {
+                uint32_t ov[2][32];
+                tmem_ld32(lane_base + kColO + c, ov[0]);
+                tmem_ld32(lane_base + kColO + c + 32, ov[1]);
                 tmem_ld_wait();
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint4 w;
-                    w.x = pack_bf16x2(__uint_as_float(ov[8 * q + 0]) * scale,
-                                      __uint_as_float(ov[8 * q + 1]) * scale);
-                    w.y = pack_bf16x2(__uint_as_float(ov[8 * q + 2]) * scale,
-                                      __uint_as_float(ov[8 * q + 3]) * scale);
-                    w.z = pack_bf16x2(__uint_as_float(ov[8 * q + 4]) * scale,
-                                      __uint_as_float(ov[8 * q + 5]) * scale);
-                    w.w = pack_bf16x2(__uint_as_float(ov[8 * q + 6]) * scale,
-                                      __uint_as_float(ov[8 * q + 7]) * scale);
-                    *reinterpret_cast<uint4 *>(qbuf + sw128_offset(row, c / 8 + q)) = w;
-                }
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(ov[h][8 * q + 0]) * scale,
+                                          __uint_as_float(ov[h][8 * q + 1]) * scale);
+                        w.y = pack_bf16x2(__uint_as_float(ov[h][8 * q + 2]) * scale,
+                                          __uint_as_float(ov[h][8 * q + 3]) * scale);
+                        w.z = pack_bf16x2(__uint_as_float(ov[h][8 * q + 4]) * scale,
+                                          __uint_as_float(ov[h][8 * q + 5]) * scale);
+                        w.w = pack_bf16x2(__uint_as_float(ov[h][8 * q + 6]) * scale,
+                                          __uint_as_float(ov[h][8 * q + 7]) * scale);
+                        *reinterpret_cast<uint4 *>(qbuf + sw128_offset(row, (c + 32 * h) / 8 + q)) = w;
+                    }
             }
             fence_proxy_async_smem();
             named_bar(1, kSoftmaxThreads);
