@@ -826,13 +826,13 @@ def time_other_configs(fga, dev, bf16_peak, hbm_peak):
 # Per-launch DRAM traffic (read + write bytes) from ncu captures of the
 # current kernels, scaled to one launch of the bench workload; None when the
 # kernels changed since the counters were taken.
-# prefill_attn_kernel: 393.4 MB read + 100.3 MB written, measured on this
-# workload (the two-issuer kernel).  decode_split_kernel: 536.9 MB read +
+# prefill_attn_kernel: 391.4 MB read + 100.1 MB written, measured on this
+# workload (the two-issuer kernel with the two-chunk epilogue).  decode_split_kernel: 536.9 MB read +
 # 3.7 MB written in a 131,072-token capture (split K/V barriers), scaled x8 to
 # the 1,048,576-token layer (the traffic grows with the cached tokens).
 TRAFFIC: dict[str, float | None] = {
     "decode_split_kernel": 540.666112e6 * 8,
-    "prefill_attn_kernel": 493.713152e6,
+    "prefill_attn_kernel": 491.444224e6,
 }
 
 
