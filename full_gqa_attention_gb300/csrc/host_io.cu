@@ -3,7 +3,7 @@
 // A caller whose inputs sit in host memory would otherwise copy the whole
 // batch in, run the prefill and copy the whole output back, one after the
 // other.  Here the batch goes through kStages device staging areas one piece
-// at a time -- a sequence, or a chunk of kHostChunk tokens of a longer one:
+// at a time -- a sequence, or a chunk (host_chunk tokens) of a longer one:
 // copy-ins of later pieces and copy-outs of earlier ones run on two copy
 // streams of the library while the caller's stream computes piece q.  A whole
 // sequence runs the prefill with B = 1; chunks run the chunked prefill over a
@@ -54,8 +54,15 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 // Sequences longer than this go through in chunks of this many tokens: the
 // chunked prefill over a device KV cache (its query tiles and, on full
-// layers, its key tiles fall where the one-shot prefill puts them).
-constexpr int kHostChunk = 2048;
+// layers, its key tiles fall where the one-shot prefill puts them).  Timed
+// on one GB300 (4B shapes, B=2, T=8192, chunks of 1024 / 2048 / 3072 / 4096
+// tokens): full layers 1.54 / 1.52 / 1.53 / 1.63 ms per call, sliding layers
+// 1.51 / 1.39 / 1.33 / 1.41 ms.  A sliding chunk costs about the same
+// wherever it sits (its keys end at the window), so longer chunks pay there;
+// a full layer's last chunks walk the whole prefix.
+int host_chunk(const spark_layer_desc *d) {
+    return d->kind == SPARK_LAYER_SLIDING ? 3072 : 2048;
+}
 constexpr int kStages = 4;        // staging areas: pieces in flight
 
 __global__ void chunk_starts_kernel(int32_t *starts, int n, int chunk) {
@@ -75,7 +82,7 @@ struct HostPlan {
 
 HostPlan plan_host(size_t core_bytes, int T, int H, int Hkv, const spark_layer_desc *desc) {
     HostPlan pl{};
-    pl.chunk = T > kHostChunk ? kHostChunk : T;
+    pl.chunk = T > host_chunk(desc) ? host_chunk(desc) : T;
     pl.nchunks = (T + pl.chunk - 1) / pl.chunk;
     pl.core_bytes = core_bytes;
     size_t off = align256(core_bytes);
@@ -113,8 +120,8 @@ extern "C" {
 
 size_t spark_attn_prefill_host_workspace_size(int B, int T, int H, int Hkv,
                                               const spark_layer_desc *desc) {
-    if (B < 0 || T < 0) return 0;
-    const int chunk = T > kHostChunk ? kHostChunk : T;
+    if (B < 0 || T < 0 || !desc) return 0;
+    const int chunk = T > host_chunk(desc) ? host_chunk(desc) : T;
     const size_t core = spark_attn_prefill_workspace_size(1, chunk, H, Hkv, desc);
     if (core == 0) return 0;
     return plan_host(core, T, H, Hkv, desc).bytes;
@@ -126,7 +133,7 @@ spark_status spark_attn_prefill_host(const void *qkv_h, const float *gate_h, con
                                      void *stream) {
     if (!desc) return SPARK_ERR_NULL;
     if (B < 0 || T < 0) return SPARK_ERR_SHAPE;
-    const int chunk0 = T > kHostChunk ? kHostChunk : T;
+    const int chunk0 = T > host_chunk(desc) ? host_chunk(desc) : T;
     const size_t core = spark_attn_prefill_workspace_size(1, chunk0, H, Hkv, desc);
     if (core == 0) {
         const spark_status st = prefill_impl(nullptr, nullptr, nullptr, desc, 1, T, H, Hkv,

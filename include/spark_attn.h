@@ -135,7 +135,8 @@ spark_status spark_attn_prefill(const void *qkv, const float *gate, const int32_
  *              is read with spark_attn_read_status)
  *
  * The batch goes through device staging areas one piece at a time -- a
- * sequence, or a chunk of 2048 tokens of a longer one (processed as a chunked
+ * sequence, or a chunk of a longer one (2048 tokens on FULL layers, 3072 on
+ * SLIDING layers; processed as a chunked
  * prefill over a device KV cache in the workspace): copy-ins of later pieces
  * and copy-outs of earlier ones run on two copy streams that the library
  * creates per device on first use, while `stream` computes.  Host buffers should be pinned

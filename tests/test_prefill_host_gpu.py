@@ -68,7 +68,7 @@ def test_host_prefill_empty_and_rejects(cuda):
 
 
 def test_host_prefill_long_sequences_full_layer_bit_exact(cuda):
-    """Sequences longer than one host chunk (2048 tokens) go through in chunks
+    """Sequences longer than one host chunk (2048 tokens on a full layer) go through in chunks
     over a device KV cache; on a full layer the chunks' query and key tiles
     fall where the one-shot prefill puts them, so the output is identical."""
     case = wl.PrefillCase("hl", B=2, T=4500, H=16, Hkv=4, layer=wl.FULL_LAYER, seed=63)
@@ -93,7 +93,8 @@ def test_host_prefill_long_sequences_sliding_layer(cuda):
                                       x["pos"].pin_memory(), case.layer)
     torch.cuda.synchronize()
     import numpy as np
-    edges = [0, 511, 512, 2047, 2048, 2049, 2559, 2560, 4095, 4096, 4499]
+    edges = [0, 511, 512, 2047, 2048, 2049, 2559, 2560, 3071, 3072, 3073, 3583, 3584, 4095,
+             4096, 4499]
     rows = np.array(sorted({b * 4500 + t for b in (0, 1) for e in edges
                             for t in range(max(0, e - 2), min(4500, e + 3))}))
     L = case.layer
