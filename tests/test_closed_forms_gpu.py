@@ -95,3 +95,58 @@ def test_shifted_positions_give_the_same_attention(cuda, layer):
                           layer.kind, layer.window, layer.theta, layer.rot_dim, H, Hkv)
     for o, name in zip(outs, ("positions 0..T-1", f"positions shifted by {shift}")):
         check_close(o, want.reshape(T, -1), name)
+
+
+def _v_row(j: int, gi: int) -> list[float]:
+    """Small integers carried by token j's value (exact in bf16 and in fp32 sums)."""
+    return [float(j & 63), float(j >> 6), 1.0, float((j * (gi + 3)) % 17)]
+
+
+@pytest.mark.parametrize("kind,W,cap,positions", [
+    (FULL, 0, 2048, [0, 1, 700, 2047]),
+    (SLIDING, 512, 512, [5, 511, 512, 1000, 1023]),
+    (SLIDING, 100, 512, [0, 99, 100, 513, 2000]),
+], ids=["full", "ring-512", "window-100-in-ring-512"])
+def test_zero_query_decode_averages_the_visible_slots(cuda, kind, W, cap, positions):
+    """Decode with a zero query: every visible slot (the new token included)
+    scores 0, so the output is the mean of the visible values.  This pins
+    which slots a step sees: all past tokens of a full layer, the latest
+    `window` tokens of a ring.  Slots no token has written hold NaN, which a
+    correct step never reads."""
+    H, Hkv = 16, 4
+    B = len(positions)
+    layer = wl.Layer(kind=kind, window=max(W, 1), theta=1e4 if kind else 5e6,
+                     rot_dim=256 if kind else 64)
+    g = torch.Generator().manual_seed(31 + cap + W)
+    kc = torch.randn((B, Hkv, cap, 256), generator=g).to(torch.bfloat16)
+    vc = torch.full((B, Hkv, cap, 256), float("nan"), dtype=torch.bfloat16)
+    qkv = torch.zeros((B, (H + 2 * Hkv) * 256), dtype=torch.float32)
+    qkv[:, H * 256:(H + Hkv) * 256] = torch.randn((B, Hkv * 256), generator=g)
+    for b, p in enumerate(positions):
+        # past tokens: slot s holds the latest token j < p with j = s (mod cap)
+        n = min(p, cap)
+        s = np.arange(n)
+        j = s if kind == FULL else s + cap * ((p - 1 - s) // cap)
+        for gi in range(Hkv):
+            rows = torch.zeros((n, 256))
+            rows[:, :4] = torch.tensor(np.array([_v_row(int(t), gi) for t in j]).reshape(n, 4))
+            vc[b, gi, :n] = rows.to(torch.bfloat16)
+            v0 = (H + Hkv + gi) * 256            # the new token's value
+            qkv[b, v0:v0 + 4] = torch.tensor(_v_row(p, gi))
+    gate = torch.full((B, H), 40.0)              # sigmoid(40) == 1.0 in fp32
+    pos = torch.tensor(positions, dtype=torch.int32)
+    out = fga.spark_attn_decode(qkv.to(torch.bfloat16).to(cuda), gate.to(cuda), pos.to(cuda),
+                                kc.to(cuda), vc.to(cuda), layer)
+    got = out.float().cpu().reshape(B, H, 256)
+    assert not torch.isnan(got).any()
+    assert float(got[:, :, 4:].abs().max()) == 0.0
+    want = np.zeros((B, Hkv, 4))
+    for b, p in enumerate(positions):
+        lo = 0 if kind == FULL else max(0, p - W + 1)
+        vis = range(lo, p + 1)
+        for gi in range(Hkv):
+            want[b, gi] = np.mean([_v_row(j, gi) for j in vis], axis=0)
+    want = np.repeat(want, H // Hkv, axis=1)
+    tol = (2.0 ** -8 + 2.0 ** -20) * np.abs(want) + 1e-7
+    diff = np.abs(got[:, :, :4].double().numpy() - want)
+    assert np.all(diff <= tol), diff.max()
