@@ -101,3 +101,33 @@ def test_host_prefill_long_sequences_sliding_layer(cuda):
     want = oracle.prefill(wl.bf16_bits(x["qkv"]), x["gate"].numpy(), x["pos"].numpy(), L.kind,
                           L.window, L.theta, L.rot_dim, 16, 4, rows=rows)
     check_close(got.reshape(9000, -1)[torch.as_tensor(rows)], want, "host prefill sliding chunks")
+
+
+@pytest.mark.parametrize("kind,T", [(wl.FULL, 2049), (wl.FULL, 4097), (wl.SLIDING, 3072),
+                                    (wl.SLIDING, 3073), (wl.SLIDING, 6200)])
+def test_host_prefill_piece_boundaries(cuda, kind, T):
+    """Lengths at the host pieces' edges: one token over a chunk (a one-token
+    last piece), exactly one sliding chunk (one piece, no cache), and several
+    sliding chunks whose ring wraps.  Rows around every piece edge and the
+    window edge are checked against the oracle."""
+    layer = wl.FULL_LAYER if kind == wl.FULL else wl.SLIDING_LAYER
+    chunk = 2048 if kind == wl.FULL else 3072
+    case = wl.PrefillCase("hb", B=1, T=T, H=16, Hkv=4, layer=layer, seed=70 + T)
+    x = wl.make_prefill_inputs(case)
+    ws = fga.new_workspace(fga.spark_attn_prefill_host_workspace_size(1, T, 16, 4, layer))
+    got = fga.spark_attn_prefill_host(x["qkv"].pin_memory(), x["gate"].pin_memory(),
+                                      x["pos"].pin_memory(), layer, workspace=ws)
+    torch.cuda.synchronize()
+    assert fga.spark_attn_read_status(ws) == 0
+    import numpy as np
+    edges = {0, 511, 512, T - 1} | {c for c in range(chunk, T, chunk)}
+    rows = np.array(sorted({t for e in edges for t in range(max(0, e - 2), min(T, e + 3))}))
+    L = case.layer
+    want = oracle.prefill(wl.bf16_bits(x["qkv"]), x["gate"].numpy(), x["pos"].numpy(), L.kind,
+                          L.window, L.theta, L.rot_dim, 16, 4, rows=rows)
+    check_close(got.reshape(T, -1)[torch.as_tensor(rows)], want, f"host prefill T={T}")
+    if kind == wl.FULL:
+        # full-layer chunks put their tiles where the one-shot prefill does
+        one = fga.spark_attn_prefill(x["qkv"].to(cuda), x["gate"].to(cuda), x["pos"].to(cuda),
+                                     layer)
+        assert torch.equal(got, one.cpu())
