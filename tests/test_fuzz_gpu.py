@@ -74,3 +74,46 @@ def test_decode_sweep(cuda, seed):
         cap = rng.choice([64, 300, 2048, 5000])
         positions = [rng.randrange(0, cap) for _ in range(rng.choice([1, 3, 5]))]
     run_case(cuda, layer, H, Hkv, cap, positions, seed=6000 + seed)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_chunked_prefill_sweep(cuda, seed):
+    """One sequence prefilled as a run of chunks of random sizes (the first at
+    start 0) over a cache whose unwritten slots hold NaN, then one decode
+    step.  Every chunk row and the decoded token are compared with the
+    oracle's prefill of the whole sequence."""
+    rng = random.Random(7000 + seed)
+    H, Hkv = rng.choice(GROUPS)
+    kind = rng.choice([wl.FULL, wl.SLIDING])
+    W = rng.choice([17, 128, 300, 512]) if kind == wl.SLIDING else 0
+    layer = wl.Layer(kind=kind, window=max(W, 1), theta=rng.choice([1e4, 5e6]),
+                     rot_dim=rng.choice([0, 16, 64, 128, 256]))
+    sizes = [rng.choice([1, 7, 64, 100, 129, 200, 333]) for _ in range(rng.choice([2, 3, 5]))]
+    total = sum(sizes)
+    if kind == wl.FULL:
+        cap = total + 1 + rng.choice([0, 5, 200])
+    else:
+        cap = (W + max(sizes) - 1 + 127) // 128 * 128 + rng.choice([0, 128])
+    case = wl.PrefillCase(f"cs{seed}", B=1, T=total + 1, H=H, Hkv=Hkv, layer=layer,
+                          seed=8000 + seed)
+    x = wl.make_prefill_inputs(case)
+    kc = torch.full((1, Hkv, cap, 256), float("nan"), dtype=torch.bfloat16, device=cuda)
+    vc = torch.full_like(kc, float("nan"))
+    outs, s0 = [], 0
+    for n in sizes:
+        sl = slice(s0, s0 + n)
+        outs.append(fga.spark_attn_prefill_chunk(
+            x["qkv"][:, sl].contiguous().to(cuda), x["gate"][:, sl].contiguous().to(cuda),
+            x["pos"][:, sl].contiguous().to(cuda), kc, vc,
+            torch.tensor([s0], dtype=torch.int32, device=cuda), layer))
+        s0 += n
+    got = torch.cat(outs, dim=1).reshape(total, -1)
+    qb = wl.bf16_bits(x["qkv"])
+    want = oracle.prefill(qb, x["gate"].numpy(), x["pos"].numpy(), layer.kind, layer.window,
+                          layer.theta, layer.rot_dim, H, Hkv)
+    want = want.reshape(total + 1, -1)
+    check_close(got, want[:total], f"chunks {sizes} cap={cap} H={H} Hkv={Hkv} {layer}")
+    y = fga.spark_attn_decode(x["qkv"][:, total].contiguous().to(cuda),
+                              x["gate"][:, total].contiguous().to(cuda),
+                              torch.tensor([total], dtype=torch.int32, device=cuda), kc, vc, layer)
+    check_close(y, want[total:], f"decode after chunks {sizes}")
