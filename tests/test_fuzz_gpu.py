@@ -117,3 +117,24 @@ def test_chunked_prefill_sweep(cuda, seed):
                               x["gate"][:, total].contiguous().to(cuda),
                               torch.tensor([total], dtype=torch.int32, device=cuda), kc, vc, layer)
     check_close(y, want[total:], f"decode after chunks {sizes}")
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_attention_block_sweep(cuda, seed):
+    """The attention block (projections around the core) over random hidden
+    sizes, lengths (few rows take the GEMV path, more the tcgen05 GEMM with
+    RoPE in its epilogue), group sizes, layer kinds and rotated widths."""
+    from test_layer_gpu import run_prefill
+    rng = random.Random(9000 + seed)
+    H, Hkv = rng.choice(GROUPS)
+    B = rng.choice([1, 2])
+    T = rng.choice([1, 3, 8, 9, 100, 129, 300])
+    hidden = rng.choice([264, 512, 1032, 2048])
+    kind = rng.choice([wl.FULL, wl.SLIDING])
+    layer = wl.Layer(kind=kind, window=rng.choice([17, 128, 512]) if kind == wl.SLIDING else 1,
+                     theta=rng.choice([1e4, 5e6]), rot_dim=rng.choice([0, 16, 64, 128, 256]),
+                     gate_mode=rng.choice([0, 0, 1]))
+    # with the silu gate the logits are kept O(1), as in the block's silu test, so that
+    # the gate factor (up to |g|) does not scale the bf16 rounding past the bar
+    run_prefill(cuda, B, T, hidden, H, Hkv, layer, seed=9500 + seed,
+                gate_scale=0.3 if layer.gate_mode == 1 else 1.0)
