@@ -78,3 +78,20 @@ def test_cuda_sources_do_not_include_the_oracle():
     for name in sorted(os.listdir(csrc)):
         text = open(os.path.join(csrc, name)).read()
         assert "spark_oracle" not in text and "oracle/" not in text, name
+
+
+def test_oracle_shares_no_code_with_the_cuda_path():
+    """The oracle includes only the C standard library and imports neither the
+    package nor anything of the CUDA path; the two meet only in the tests."""
+    odir = os.path.join(ROOT, "oracle")
+    std = {"math.h", "stdint.h", "stdlib.h", "string.h", "stdio.h", "float.h", "omp.h"}
+    for name in sorted(os.listdir(odir)):
+        path = os.path.join(odir, name)
+        if name.endswith(".c"):
+            for line in open(path):
+                if line.lstrip().startswith("#include"):
+                    header = line.split("#include", 1)[1].strip().strip("<>\"")
+                    assert header in std, (name, header)
+        elif name.endswith(".py"):
+            mods = _imported_modules(path)
+            assert "full_gqa_attention_gb300" not in mods and "workloads" not in mods, (name, mods)
