@@ -861,7 +861,7 @@ def oracle_prefill_rows(case, n_rows: int, seed: int = 0):
     """Times the fp64 oracle on n_rows random query rows (all heads) of a
     prefill workload, or on all of it when n_rows >= B*T.  Returns (seconds,
     algorithmic flops of those rows, fraction of the workload's flops,
-    description)."""
+    description, the rows (None: all), the oracle's output for them)."""
     import numpy as np
     import oracle
     x, bits = _prefill_inputs(case)
@@ -877,16 +877,40 @@ def oracle_prefill_rows(case, n_rows: int, seed: int = 0):
         vis = _visible(rows % case.T, case).sum()
         desc = f"{n_rows} random query rows (all {case.H} heads) of {case.name}"
     t0 = time.perf_counter()
-    oracle.prefill(bits, x["gate"].numpy(), x["pos"].numpy(), L.kind, L.window, L.theta,
-                   L.rot_dim, case.H, case.Hkv, rows=rows, gate_mode=L.gate_mode)
+    want = oracle.prefill(bits, x["gate"].numpy(), x["pos"].numpy(), L.kind, L.window, L.theta,
+                          L.rot_dim, case.H, case.Hkv, rows=rows, gate_mode=L.gate_mode)
     dt = time.perf_counter() - t0
     flops = 4.0 * 256 * case.H * float(vis)
-    return dt, flops, flops / prefill_flops(case), desc
+    return dt, flops, flops / prefill_flops(case), desc, rows, want
+
+
+def prefill_parity(case, rows, want):
+    """The library's output for the same workload against the oracle rows
+    just timed: max-abs and rel-L2 over every element of those rows, beside
+    the bar the tests hold it to (max-abs <= 2e-2, rel-L2 <= 1e-2 against
+    fp64).  Only the CPU-baseline leg calls this."""
+    import numpy as np
+    import torch
+    import full_gqa_attention_gb300 as fga
+    x, _ = _prefill_inputs(case)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    out = fga.spark_attn_prefill(x["qkv"].to(dev), x["gate"].to(dev), x["pos"].to(dev),
+                                 case.layer)
+    got = out.reshape(case.B * case.T, -1)
+    if rows is not None:
+        got = got[torch.as_tensor(rows, device=dev)]
+    got = got.float().cpu().double().numpy()
+    want = np.asarray(want, dtype=np.float64).reshape(got.shape)
+    max_abs = float(np.abs(got - want).max())
+    rel_l2 = float(np.linalg.norm(got - want) / max(np.linalg.norm(want), 1e-30))
+    return {"rows": int(got.shape[0]), "max_abs": max_abs, "rel_l2": rel_l2,
+            "bar": {"max_abs": 2e-2, "rel_l2": 1e-2},
+            "ok": bool(max_abs <= 2e-2 and rel_l2 <= 1e-2)}
 
 
 def oracle_prefill_sample(n_rows: int, seed: int = 0):
     """The oracle on n_rows random query rows of the benchmark's prefill."""
-    dt, flops, _, desc = oracle_prefill_rows(PREFILL, n_rows, seed)
+    dt, flops, _, desc, _, _ = oracle_prefill_rows(PREFILL, n_rows, seed)
     return dt, flops, desc
 
 
@@ -901,18 +925,70 @@ def _sized(run, target_s: float, n0: int, n_max: int):
         n = min(n_max, int(n * min(8.0, max(2.0, 1.5 * target_s / max(res[0], 1e-3)))))
 
 
-def oracle_decode_time(case, positions, k_bits, v_bits):
+def oracle_decode_time(case, positions, k_bits, v_bits, parity=None, step=None, k_dev=None,
+                       v_dev=None):
     """Seconds the fp64 oracle takes for one decode step of the given
-    sequences (qkv / gate from the workload's seeded step inputs)."""
+    sequences (qkv / gate from `step`, else the workload's seeded step
+    inputs).  With a ParityTally, the library's decode of the same step on the
+    same caches (device copies of k_bits / v_bits, or k_dev / v_dev as they
+    are) is compared with the oracle's output."""
     import numpy as np
     import oracle
-    step = wl.make_decode_step_inputs(wl.scaled(case, B=len(positions)))
+    if step is None:
+        step = wl.make_decode_step_inputs(wl.scaled(case, B=len(positions)))
     L = case.layer
     pos = np.asarray(positions, np.int32)
     t0 = time.perf_counter()
-    oracle.decode(wl.bf16_bits(step["qkv"]), step["gate"].numpy(), pos, k_bits, v_bits, L.kind,
-                  L.window, L.theta, L.rot_dim, case.H, case.Hkv, gate_mode=L.gate_mode)
-    return time.perf_counter() - t0
+    want, _, _ = oracle.decode(wl.bf16_bits(step["qkv"]), step["gate"].numpy(), pos, k_bits,
+                               v_bits, L.kind, L.window, L.theta, L.rot_dim, case.H, case.Hkv,
+                               gate_mode=L.gate_mode)
+    dt = time.perf_counter() - t0
+    if parity is not None:
+        parity.add(decode_on_device(case, step, pos, k_bits, v_bits, k_dev, v_dev), want)
+    return dt
+
+
+class ParityTally:
+    """max-abs and rel-L2 of the library's outputs against the oracle's, over
+    every element compared (the tests' bar: max-abs <= 2e-2, rel-L2 <= 1e-2
+    against fp64).  Only the CPU-baseline leg uses it."""
+
+    def __init__(self):
+        self.n, self.max_abs, self.err2, self.ref2 = 0, 0.0, 0.0, 0.0
+
+    def add(self, got, want):
+        import numpy as np
+        got = np.asarray(got, np.float64).reshape(-1)
+        want = np.asarray(want, np.float64).reshape(-1)
+        d = got - want
+        self.n += 1
+        self.max_abs = max(self.max_abs, float(np.abs(d).max()))
+        self.err2 += float(d @ d)
+        self.ref2 += float(want @ want)
+
+    def result(self, what):
+        rel = (self.err2 / self.ref2) ** 0.5 if self.ref2 > 0 else 0.0
+        return {what: self.n, "max_abs": self.max_abs, "rel_l2": rel,
+                "bar": {"max_abs": 2e-2, "rel_l2": 1e-2},
+                "ok": bool(self.max_abs <= 2e-2 and rel <= 1e-2)}
+
+
+def decode_on_device(case, step, pos, k_bits, v_bits, k_dev=None, v_dev=None):
+    """The library's decode of one step, on device copies of the given caches
+    (or on device caches given as they are); returns the output as float64."""
+    import numpy as np
+    import torch
+    import full_gqa_attention_gb300 as fga
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if k_dev is None:
+        k_dev = torch.from_numpy(np.ascontiguousarray(k_bits).view(np.int16)).view(
+            torch.bfloat16).to(dev)
+        v_dev = torch.from_numpy(np.ascontiguousarray(v_bits).view(np.int16)).view(
+            torch.bfloat16).to(dev)
+    out = fga.spark_attn_decode(step["qkv"].to(dev), step["gate"].to(dev),
+                                torch.as_tensor(pos, dtype=torch.int32).to(dev), k_dev, v_dev,
+                                case.layer)
+    return out.float().cpu().double().numpy()
 
 
 def _cpu_cache(B, Hkv, n, seed):
@@ -929,7 +1005,7 @@ def oracle_decode_batched(case, n_seq: int, seed: int = 0):
     """The oracle on n_seq of the batched decode workload's sequences (all 64
     when n_seq >= B), each at its own length, caches seeded on the host.
     Returns (seconds, KV bytes read, fraction of the workload's KV bytes,
-    description)."""
+    description, parity of the library's decode of the same sequences)."""
     import numpy as np
     lengths = wl.make_decode_lengths(case).numpy().astype(np.int64)
     if n_seq >= case.B:
@@ -938,24 +1014,26 @@ def oracle_decode_batched(case, n_seq: int, seed: int = 0):
         seqs = np.sort(np.random.default_rng(seed).choice(case.B, n_seq, replace=False))
     visible = lambda p: (p + 1) if case.layer.kind == wl.FULL else min(p + 1, case.layer.window)  # noqa: E731
     dt, kv = 0.0, 0
+    tally = ParityTally()
     if case.layer.kind == wl.SLIDING:
         # rings: every sequence in one oracle call
         pos = lengths[seqs]
         k = _cpu_cache(len(seqs), case.Hkv, case.cap, seed + 1)
         v = _cpu_cache(len(seqs), case.Hkv, case.cap, seed + 2)
-        dt = oracle_decode_time(case, pos, k, v)
+        dt = oracle_decode_time(case, pos, k, v, tally)
         kv = sum(visible(int(p)) for p in pos) * KV_BYTES_PER_TOKEN
     else:
         for i, b in enumerate(seqs):
             p = int(lengths[b])
             k = _cpu_cache(1, case.Hkv, p + 1, seed + 3 * i + 1)
             v = _cpu_cache(1, case.Hkv, p + 1, seed + 3 * i + 2)
-            dt += oracle_decode_time(case, [p], k, v)
+            dt += oracle_decode_time(case, [p], k, v, tally)
             kv += visible(p) * KV_BYTES_PER_TOKEN
             del k, v
     total = sum(visible(int(p)) for p in lengths) * KV_BYTES_PER_TOKEN
     what = "all" if len(seqs) == case.B else f"{len(seqs)} seeded-random"
-    return dt, kv, kv / total, f"{what} of the {case.B} sequences of {case.name}"
+    return (dt, kv, kv / total, f"{what} of the {case.B} sequences of {case.name}",
+            tally.result("calls"))
 
 
 def oracle_decode_1m(dec):
@@ -963,12 +1041,14 @@ def oracle_decode_1m(dec):
     back from the benchmark's own device copy) and one sliding layer of the
     1M-context decode step; the 36-layer step is extrapolated as 9 full + 27
     sliding layers.  Returns (step seconds extrapolated, KV bytes of the
-    step, seconds measured, description)."""
+    step, seconds measured, description, parity of the library's decode of
+    those two layers against the oracle's)."""
     full = next((L for L in dec if L["layer"].kind == wl.FULL), None)
     slid = next((L for L in dec if L["layer"].kind == wl.SLIDING), None)
     n_full = sum(1 for L in dec if L["layer"].kind == wl.FULL)
     n_slid = len(dec) - n_full
     measured, t_full, t_slid = 0.0, 0.0, 0.0
+    tally = ParityTally()
     for L, kind in ((full, "full"), (slid, "sliding")):
         if L is None:
             continue
@@ -977,7 +1057,10 @@ def oracle_decode_1m(dec):
         n = min(p + 1, c.cap) if kind == "full" else c.cap
         k = wl.bf16_bits(L["k"][:, :, :n].cpu())
         v = wl.bf16_bits(L["v"][:, :, :n].cpu())
-        t = oracle_decode_time(c, [p], k, v)
+        # the layer's own step inputs; the library's decode of the same step runs
+        # on the benchmark's own caches (each step rewrites slot p with the same
+        # key and value)
+        t = oracle_decode_time(c, [p], k, v, tally, step=L["host"], k_dev=L["k"], v_dev=L["v"])
         del k, v
         measured += t
         if kind == "full":
@@ -988,7 +1071,7 @@ def oracle_decode_1m(dec):
     kv, _ = decode_kv_bytes([L["layer"] for L in dec])
     return step_s, kv, measured, (f"one full layer (1,048,575 cached tokens) and one sliding "
                                   f"layer, extrapolated to the {n_full} + {n_slid} layers of "
-                                  "the step")
+                                  "the step"), tally.result("layers")
 
 
 def cpu_threads() -> int:
@@ -1013,12 +1096,13 @@ def cpu_baseline(args, dec=None):
     def prefill_entry(case, target_s, n0):
         total_rows = case.B * case.T
         if target_s is None:
-            dt, flops, frac, desc = oracle_prefill_rows(case, total_rows)
+            dt, flops, frac, desc, rows, want = oracle_prefill_rows(case, total_rows)
         else:
-            dt, flops, frac, desc = _sized(lambda n: oracle_prefill_rows(case, n), target_s,
-                                           n0, total_rows)
+            dt, flops, frac, desc, rows, want = _sized(lambda n: oracle_prefill_rows(case, n),
+                                                       target_s, n0, total_rows)
         e = {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-             "sample": desc + f", {dt:.2f} s", "seconds": dt}
+             "sample": desc + f", {dt:.2f} s", "seconds": dt,
+             "parity": prefill_parity(case, rows, want)}
         if frac < 1.0:
             e["workload_seconds_extrapolated"] = dt / frac
         return e
@@ -1030,18 +1114,18 @@ def cpu_baseline(args, dec=None):
     per["long_prefill_sliding_T65536"] = prefill_entry(wl.PREFILL_SLIDING_4B_T65536, 3.0, 256)
     for key, case, n in (("batched_decode_full_B64", wl.DECODE_FULL_4B_B64, 8),
                          ("batched_decode_sliding_B64", wl.DECODE_SLIDING_4B_B64, 64)):
-        dt, kv, frac, desc = oracle_decode_batched(case, n)
+        dt, kv, frac, desc, par = oracle_decode_batched(case, n)
         e = {"value": kv / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
-             "sample": desc + f", {dt:.2f} s", "seconds": dt}
+             "sample": desc + f", {dt:.2f} s", "seconds": dt, "parity": par}
         if frac < 1.0:
             e["workload_seconds_extrapolated"] = dt / frac
         per[key] = e
     if dec:
-        step_s, kv, measured, desc = oracle_decode_1m(dec)
+        step_s, kv, measured, desc, par = oracle_decode_1m(dec)
         per["decode_step_1m_36_layers"] = {
             "value": kv / step_s / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": desc + f", {measured:.2f} s measured", "seconds": measured,
-            "workload_seconds_extrapolated": step_s}
+            "workload_seconds_extrapolated": step_s, "parity": par}
     head = per["prefill_4b_full_B2_T8192"]
     return {"value": head["value"], "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": head["sample"], "per_config": per}
